@@ -1,0 +1,225 @@
+"""ctypes binding of libstreamkl (argument marshalling only).
+
+Every step of the computation runs in the CUDA kernels of ``libstreamkl.so``;
+this module only checks tensor metadata, allocates outputs and workspaces
+through PyTorch's CUDA allocator, and passes raw pointers and the current CUDA
+stream to the C entry points of the same names.  There is no CPU fallback: if
+the library is missing, every call raises.
+
+Inputs given as CPU tensors are copied to the current CUDA device on the
+current stream (non-blocking from pinned memory) and the results are copied
+back, so a host caller uses the same functions.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libstreamkl.so")
+
+OK, ERR_INVALID, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT = range(6)
+BWD_AUTO, BWD_FUSED, BWD_SEPARATE, BWD_DQ_ONLY, BWD_DK_ONLY = 0, 1, 2, 3, 4
+SPLITK_MAX_NQ = 16
+
+
+class Shape(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int), ("H", ctypes.c_int), ("NQ", ctypes.c_int), ("NK", ctypes.c_int),
+                ("D", ctypes.c_int), ("scale", ctypes.c_float), ("causal", ctypes.c_int)]
+
+
+class StreamKLError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} (status {status})")
+
+
+_P, _F, _S, _I, _SZ = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+# name -> (restype, argtypes); also the list of symbols include/streamkl.h declares
+SIGNATURES = {
+    "streamkl_fwd": (_I, [_P, _P, _P, _P, Shape, _F, _F, _F, _S]),
+    "streamkl_fwd_splitk_workspace": (_I, [Shape, _I, ctypes.POINTER(_SZ)]),
+    "streamkl_fwd_splitk": (_I, [_P, _P, _P, _P, Shape, _I, _P, _SZ, _F, _F, _F, _S]),
+    "streamkl_fwd_splitk_plan": (_I, [Shape, _I, ctypes.POINTER(_I)]),
+    "streamkl_bwd_workspace": (_I, [Shape, _I, ctypes.POINTER(_SZ)]),
+    "streamkl_bwd_select": (_I, [Shape, _SZ]),
+    "streamkl_bwd_s1": (_I, [_P, _P, _P, _P, Shape, _F, _F, _F, _P, _P, _I, _P, _SZ, _S]),
+    "streamkl_bwd_s2": (_I, [_P, _P, _P, _P, Shape, _F, _F, _F, _F, _P, _P, _I, _P, _SZ, _S]),
+    "streamkl_status_string": (ctypes.c_char_p, [_I]),
+    "streamkl_check_device_status": (_I, [_S]),
+    "streamkl_debug_wait_timeout": (_I, [_I, _S]),
+    "streamkl_version": (_I, []),
+}
+
+_lib: Optional[ctypes.CDLL] = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libstreamkl.so not found at {LIB_PATH}: build it with "
+                               "attention_kl_divergence_streamkl_gb300.build.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().streamkl_status_string(int(status)).decode()
+
+
+def _check(status: int, where: str) -> None:
+    if status != OK:
+        raise StreamKLError(status, where)
+
+
+def make_shape(B, H, NQ, NK, D, scale=None, causal=False) -> Shape:
+    return Shape(int(B), int(H), int(NQ), int(NK), int(D), float(scale or 0.0), int(bool(causal)))
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device: torch.device):
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _prep(q1, k1, q2, k2):
+    """Validates the four inputs; returns (device tensors, shape, was_host)."""
+    ts = [q1, k1, q2, k2]
+    for t in ts:
+        if t.dtype != torch.bfloat16:
+            raise TypeError("Q1, K1, Q2, K2 must be bfloat16")
+        if t.dim() != 4:
+            raise ValueError("Q1, K1, Q2, K2 must be [B, H, N, D]")
+    if q1.shape != q2.shape or k1.shape != k2.shape or q1.shape[:2] != k1.shape[:2] or q1.shape[3] != k1.shape[3]:
+        raise ValueError(f"shape mismatch: Q1 {tuple(q1.shape)} K1 {tuple(k1.shape)} "
+                         f"Q2 {tuple(q2.shape)} K2 {tuple(k2.shape)}")
+    host = q1.device.type == "cpu"
+    if host:
+        dev = torch.device("cuda", torch.cuda.current_device())
+        ts = [t.contiguous().to(dev, non_blocking=True) for t in ts]
+    else:
+        ts = [t.contiguous() for t in ts]
+        if any(t.device != ts[0].device for t in ts):
+            raise ValueError("inputs on different devices")
+    return ts, host
+
+
+def _rows(t: Optional[torch.Tensor], dev, shape3, name):
+    if t is None:
+        return None
+    if t.dtype != torch.float32 or tuple(t.shape) != tuple(shape3):
+        raise ValueError(f"{name} must be float32 of shape {tuple(shape3)}")
+    return t.to(dev, non_blocking=True).contiguous()
+
+
+def _back(ts, host):
+    if not host:
+        return ts
+    out = tuple(t.to("cpu", non_blocking=True) for t in ts)
+    torch.cuda.current_stream().synchronize()
+    return out
+
+
+def fwd(q1, k1, q2, k2, scale=None, causal=False):
+    """KL, LSE1, LSE2 fp32 [B, H, N_Q] (one-pass forward)."""
+    (q1, k1, q2, k2), host = _prep(q1, k1, q2, k2)
+    B, H, NQ, D = q1.shape
+    s = make_shape(B, H, NQ, k1.shape[2], D, scale, causal)
+    kl, l1, l2 = (torch.empty((B, H, NQ), dtype=torch.float32, device=q1.device) for _ in range(3))
+    _check(lib().streamkl_fwd(_ptr(q1), _ptr(k1), _ptr(q2), _ptr(k2), s, _ptr(kl), _ptr(l1), _ptr(l2),
+                              _stream(q1.device)), "streamkl_fwd")
+    return _back((kl, l1, l2), host)
+
+
+def splitk_plan(B, H, NQ, NK, D, num_sms=0, causal=False) -> int:
+    n = ctypes.c_int(0)
+    _check(lib().streamkl_fwd_splitk_plan(make_shape(B, H, NQ, NK, D, None, causal), int(num_sms),
+                                          ctypes.byref(n)), "streamkl_fwd_splitk_plan")
+    return n.value
+
+
+def fwd_splitk(q1, k1, q2, k2, scale=None, causal=False, num_splits=0):
+    """Split-K forward for N_Q <= 16: KL, LSE1, LSE2 fp32 [B, H, N_Q]."""
+    (q1, k1, q2, k2), host = _prep(q1, k1, q2, k2)
+    B, H, NQ, D = q1.shape
+    s = make_shape(B, H, NQ, k1.shape[2], D, scale, causal)
+    nbytes = ctypes.c_size_t(0)
+    _check(lib().streamkl_fwd_splitk_workspace(s, int(num_splits), ctypes.byref(nbytes)),
+           "streamkl_fwd_splitk_workspace")
+    ws = torch.empty(max(16, nbytes.value), dtype=torch.uint8, device=q1.device)
+    kl, l1, l2 = (torch.empty((B, H, NQ), dtype=torch.float32, device=q1.device) for _ in range(3))
+    _check(lib().streamkl_fwd_splitk(_ptr(q1), _ptr(k1), _ptr(q2), _ptr(k2), s, int(num_splits), _ptr(ws),
+                                     nbytes.value, _ptr(kl), _ptr(l1), _ptr(l2), _stream(q1.device)),
+           "streamkl_fwd_splitk")
+    return _back((kl, l1, l2), host)
+
+
+def bwd_select(B, H, NQ, NK, D, l2_bytes, causal=False) -> int:
+    return lib().streamkl_bwd_select(make_shape(B, H, NQ, NK, D, None, causal), int(l2_bytes))
+
+
+def bwd_workspace_bytes(B, H, NQ, NK, D, bwd_mode=BWD_AUTO, causal=False) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib().streamkl_bwd_workspace(make_shape(B, H, NQ, NK, D, None, causal), int(bwd_mode),
+                                        ctypes.byref(n)), "streamkl_bwd_workspace")
+    return n.value
+
+
+def _bwd(setting, q1, k1, q2, k2, lse1, lse2, kl, g, scale, causal, bwd_mode):
+    (q1, k1, q2, k2), host = _prep(q1, k1, q2, k2)
+    B, H, NQ, D = q1.shape
+    NK = k1.shape[2]
+    dev = q1.device
+    s = make_shape(B, H, NQ, NK, D, scale, causal)
+    lse1 = _rows(lse1, dev, (B, H, NQ), "lse1")
+    lse2 = _rows(lse2, dev, (B, H, NQ), "lse2")
+    g = _rows(g, dev, (B, H, NQ), "g")
+    kl = _rows(kl, dev, (B, H, NQ), "kl") if setting == 2 else None
+    nbytes = ctypes.c_size_t(0)
+    _check(lib().streamkl_bwd_workspace(s, int(bwd_mode), ctypes.byref(nbytes)), "streamkl_bwd_workspace")
+    ws = torch.empty(max(16, nbytes.value), dtype=torch.uint8, device=dev)
+    dq = torch.empty((B, H, NQ, D), dtype=torch.bfloat16, device=dev) if bwd_mode != BWD_DK_ONLY else None
+    dk = torch.empty((B, H, NK, D), dtype=torch.bfloat16, device=dev) if bwd_mode != BWD_DQ_ONLY else None
+    if setting == 1:
+        st = lib().streamkl_bwd_s1(_ptr(q1), _ptr(k1), _ptr(q2), _ptr(k2), s, _ptr(lse1), _ptr(lse2), _ptr(g),
+                                   _ptr(dq), _ptr(dk), int(bwd_mode), _ptr(ws), nbytes.value, _stream(dev))
+    else:
+        st = lib().streamkl_bwd_s2(_ptr(q1), _ptr(k1), _ptr(q2), _ptr(k2), s, _ptr(lse1), _ptr(lse2), _ptr(kl),
+                                   _ptr(g), _ptr(dq), _ptr(dk), int(bwd_mode), _ptr(ws), nbytes.value,
+                                   _stream(dev))
+    _check(st, f"streamkl_bwd_s{setting}")
+    got = iter(_back(tuple(t for t in (dq, dk) if t is not None), host))
+    return tuple(None if t is None else next(got) for t in (dq, dk))
+
+
+def bwd_s1(q1, k1, q2, k2, lse1, lse2, g, scale=None, causal=False, bwd_mode=BWD_AUTO):
+    """Setting 1 (P1 fixed): (dQ2, dK2) bf16."""
+    return _bwd(1, q1, k1, q2, k2, lse1, lse2, None, g, scale, causal, bwd_mode)
+
+
+def bwd_s2(q1, k1, q2, k2, lse1, lse2, kl, g, scale=None, causal=False, bwd_mode=BWD_AUTO):
+    """Setting 2 (P2 fixed): (dQ1, dK1) bf16."""
+    return _bwd(2, q1, k1, q2, k2, lse1, lse2, kl, g, scale, causal, bwd_mode)
+
+
+def check_device_status(device=None) -> int:
+    """Synchronises the current stream and returns (and clears) the device status."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    return lib().streamkl_check_device_status(_stream(dev))
+
+
+def debug_wait_timeout(timeout_us: int) -> int:
+    dev = torch.device("cuda", torch.cuda.current_device())
+    return lib().streamkl_debug_wait_timeout(int(timeout_us), _stream(dev))

@@ -1,0 +1,289 @@
+// C-ABI of libstreamkl: argument validation, path selection and launches.
+// The operations are declared and documented in include/streamkl.h.
+#include <math.h>
+#include <stdint.h>
+
+#include "../../include/streamkl.h"
+#include "common.cuh"
+#include "kernels.h"
+
+// Device status word: bounded waits that run out OR bits into it.
+__device__ int g_streamkl_status;
+
+namespace skl {
+
+namespace {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  // Resolved once; every thread that races here stores the same pointer.
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  }
+  return fn;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Maximum key/query tiles along grid.y.
+constexpr long long kMaxGridY = 65535;
+constexpr int kMaxRows = 1 << 30;
+
+streamkl_status validate(const streamkl_shape& s, Problem* p) {
+  if (s.B <= 0 || s.H <= 0 || s.NQ < 0 || s.NK <= 0 || s.D <= 0) return STREAMKL_ERR_INVALID;
+  if (!(s.scale == s.scale) || isinf(s.scale)) return STREAMKL_ERR_INVALID;
+  if (s.causal && s.NQ > s.NK) return STREAMKL_ERR_INVALID;
+  if (s.NQ > kMaxRows || s.NK > kMaxRows) return STREAMKL_ERR_UNSUPPORTED;
+  if ((long long)s.B * s.H > 0x7fffffffLL) return STREAMKL_ERR_UNSUPPORTED;
+  if (s.D != 64 && s.D != 128) return STREAMKL_ERR_UNSUPPORTED;
+  if ((s.NQ + 127LL) / 128 > kMaxGridY || (s.NK + 127LL) / 128 > kMaxGridY) return STREAMKL_ERR_UNSUPPORTED;
+  p->B = s.B;
+  p->H = s.H;
+  p->NQ = s.NQ;
+  p->NK = s.NK;
+  p->D = s.D;
+  p->BH = s.B * s.H;
+  p->causal = s.causal ? 1 : 0;
+  p->off = s.NK - s.NQ;
+  p->scale = s.scale > 0.f ? s.scale : 1.0f / sqrtf((float)s.D);
+  p->c = p->scale * kLog2e;
+  return STREAMKL_OK;
+}
+
+bool inputs_ok(const void* q1, const void* k1, const void* q2, const void* k2) {
+  return q1 && k1 && q2 && k2 && aligned16(q1) && aligned16(k1) && aligned16(q2) && aligned16(k2);
+}
+
+bool rows_ok(const float* a) { return a && (reinterpret_cast<uintptr_t>(a) & 3u) == 0; }
+
+streamkl_status status_ptr(int** out) {
+  if (cudaGetSymbolAddress(reinterpret_cast<void**>(out), g_streamkl_status) != cudaSuccess) return STREAMKL_ERR_CUDA;
+  return STREAMKL_OK;
+}
+
+streamkl_status from_cuda(cudaError_t e) { return e == cudaSuccess ? STREAMKL_OK : STREAMKL_ERR_CUDA; }
+
+size_t dq_acc_bytes(const Problem& p) { return (size_t)p.BH * p.NQ * p.D * sizeof(float); }
+
+int resolve_bwd_mode(const Problem& p, int mode, size_t l2_bytes) {
+  if (mode == STREAMKL_BWD_FUSED || mode == STREAMKL_BWD_SEPARATE) return mode;
+  return dq_acc_bytes(p) <= l2_bytes ? STREAMKL_BWD_FUSED : STREAMKL_BWD_SEPARATE;
+}
+
+streamkl_status device_l2_bytes(size_t* out) {
+  int dev = 0, l2 = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return STREAMKL_ERR_CUDA;
+  if (cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev) != cudaSuccess) return STREAMKL_ERR_CUDA;
+  *out = (size_t)l2;
+  return STREAMKL_OK;
+}
+
+streamkl_status device_sms(int* out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return STREAMKL_ERR_CUDA;
+  if (cudaDeviceGetAttribute(out, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return STREAMKL_ERR_CUDA;
+  return STREAMKL_OK;
+}
+
+// Bounded wait on a barrier that nothing arrives at: exercises the timeout path.
+__global__ void wait_timeout_probe_kernel(unsigned long long limit_ns, int* status) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(smem_u32(&bar), 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_wait(smem_u32(&bar), 0, status, &abort_flag, limit_ns);
+}
+
+}  // namespace
+
+bool encode_tile_map(CUtensorMap* map, const void* base, int D, int N, int BH, int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)N, (cuuint64_t)BH};
+  const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)N * D * 2};
+  const cuuint32_t box[3] = {64u, (cuuint32_t)box_rows, 1u};
+  const cuuint32_t estr[3] = {1u, 1u, 1u};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+cudaError_t launch_wait_timeout_probe(int timeout_us, int* status, cudaStream_t st) {
+  wait_timeout_probe_kernel<<<1, 32, 0, st>>>((unsigned long long)timeout_us * 1000ull, status);
+  return cudaGetLastError();
+}
+
+}  // namespace skl
+
+using namespace skl;
+
+extern "C" {
+
+int streamkl_version(void) { return 100; }
+
+const char* streamkl_status_string(streamkl_status st) {
+  switch (st) {
+    case STREAMKL_OK: return "ok";
+    case STREAMKL_ERR_INVALID: return "invalid argument";
+    case STREAMKL_ERR_UNSUPPORTED: return "unsupported shape or option";
+    case STREAMKL_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case STREAMKL_ERR_CUDA: return "CUDA call failed";
+    case STREAMKL_ERR_TIMEOUT: return "device-side wait timed out";
+  }
+  return "unknown status";
+}
+
+streamkl_status streamkl_fwd(const void* q1, const void* k1, const void* q2, const void* k2, streamkl_shape s,
+                             float* kl, float* lse1, float* lse2, void* stream) {
+  Problem p;
+  streamkl_status v = validate(s, &p);
+  if (v != STREAMKL_OK) return v;
+  if (p.NQ == 0) return STREAMKL_OK;
+  if (!inputs_ok(q1, k1, q2, k2) || !rows_ok(kl) || !rows_ok(lse1) || !rows_ok(lse2)) return STREAMKL_ERR_INVALID;
+  int* status = nullptr;
+  if ((v = status_ptr(&status)) != STREAMKL_OK) return v;
+  return from_cuda(launch_fwd(p, q1, k1, q2, k2, kl, lse1, lse2, status, static_cast<cudaStream_t>(stream)));
+}
+
+streamkl_status streamkl_fwd_splitk_plan(streamkl_shape s, int num_sms, int* num_splits) {
+  Problem p;
+  streamkl_status v = validate(s, &p);
+  if (v != STREAMKL_OK) return v;
+  if (!num_splits) return STREAMKL_ERR_INVALID;
+  if (num_sms <= 0 && (v = device_sms(&num_sms)) != STREAMKL_OK) return v;
+  int sp = splitk_plan(p.BH, splitk_key_tiles(p), num_sms);
+  *num_splits = sp > (int)kMaxGridY ? (int)kMaxGridY : sp;
+  return STREAMKL_OK;
+}
+
+streamkl_status streamkl_fwd_splitk_workspace(streamkl_shape s, int num_splits, size_t* bytes) {
+  Problem p;
+  streamkl_status v = validate(s, &p);
+  if (v != STREAMKL_OK) return v;
+  if (!bytes || num_splits < 0 || num_splits > kMaxGridY) return STREAMKL_ERR_INVALID;
+  if (p.NQ > STREAMKL_SPLITK_MAX_NQ) return STREAMKL_ERR_UNSUPPORTED;
+  if (num_splits == 0 && (v = streamkl_fwd_splitk_plan(s, 0, &num_splits)) != STREAMKL_OK) return v;
+  *bytes = (size_t)p.BH * p.NQ * num_splits * 5 * sizeof(float);
+  return STREAMKL_OK;
+}
+
+streamkl_status streamkl_fwd_splitk(const void* q1, const void* k1, const void* q2, const void* k2,
+                                    streamkl_shape s, int num_splits, void* workspace, size_t workspace_bytes,
+                                    float* kl, float* lse1, float* lse2, void* stream) {
+  Problem p;
+  streamkl_status v = validate(s, &p);
+  if (v != STREAMKL_OK) return v;
+  if (p.NQ > STREAMKL_SPLITK_MAX_NQ) return STREAMKL_ERR_UNSUPPORTED;
+  if (num_splits < 0 || num_splits > kMaxGridY) return STREAMKL_ERR_INVALID;
+  if (p.NQ == 0) return STREAMKL_OK;
+  if (!inputs_ok(q1, k1, q2, k2) || !rows_ok(kl) || !rows_ok(lse1) || !rows_ok(lse2)) return STREAMKL_ERR_INVALID;
+  if (num_splits == 0 && (v = streamkl_fwd_splitk_plan(s, 0, &num_splits)) != STREAMKL_OK) return v;
+  const size_t need = (size_t)p.BH * p.NQ * num_splits * 5 * sizeof(float);
+  if (!workspace || !aligned16(workspace) || workspace_bytes < need) return STREAMKL_ERR_WORKSPACE;
+  int* status = nullptr;
+  if ((v = status_ptr(&status)) != STREAMKL_OK) return v;
+  return from_cuda(launch_splitk(p, q1, k1, q2, k2, num_splits, static_cast<float*>(workspace), kl, lse1, lse2,
+                                 status, static_cast<cudaStream_t>(stream)));
+}
+
+int streamkl_bwd_select(streamkl_shape s, size_t l2_bytes) {
+  Problem p;
+  if (validate(s, &p) != STREAMKL_OK) return 0;
+  return resolve_bwd_mode(p, STREAMKL_BWD_AUTO, l2_bytes);
+}
+
+streamkl_status streamkl_bwd_workspace(streamkl_shape s, int bwd_mode, size_t* bytes) {
+  Problem p;
+  streamkl_status v = validate(s, &p);
+  if (v != STREAMKL_OK) return v;
+  if (!bytes || bwd_mode < 0 || bwd_mode > STREAMKL_BWD_DK_ONLY) return STREAMKL_ERR_INVALID;
+  if (bwd_mode == STREAMKL_BWD_AUTO) {
+    size_t l2 = 0;
+    if ((v = device_l2_bytes(&l2)) != STREAMKL_OK) return v;
+    bwd_mode = resolve_bwd_mode(p, bwd_mode, l2);
+  }
+  *bytes = bwd_mode == STREAMKL_BWD_FUSED ? dq_acc_bytes(p) : 0;
+  return STREAMKL_OK;
+}
+
+static streamkl_status bwd_common(int setting, const void* q1, const void* k1, const void* q2, const void* k2,
+                                  streamkl_shape s, const float* lse1, const float* lse2, const float* kl,
+                                  const float* g, void* dq, void* dk, int bwd_mode, void* workspace,
+                                  size_t workspace_bytes, void* stream) {
+  Problem p;
+  streamkl_status v = validate(s, &p);
+  if (v != STREAMKL_OK) return v;
+  if (bwd_mode < 0 || bwd_mode > STREAMKL_BWD_DK_ONLY) return STREAMKL_ERR_INVALID;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const bool want_dq = bwd_mode != STREAMKL_BWD_DK_ONLY;
+  const bool want_dk = bwd_mode != STREAMKL_BWD_DQ_ONLY;
+  if (want_dk && (!dk || !aligned16(dk))) return STREAMKL_ERR_INVALID;
+  if (p.NQ == 0) {
+    // no query rows: the loss is an empty sum, so dK is zero
+    return want_dk ? from_cuda(cudaMemsetAsync(dk, 0, (size_t)p.BH * p.NK * p.D * 2, st)) : STREAMKL_OK;
+  }
+  if (!inputs_ok(q1, k1, q2, k2) || !rows_ok(lse1) || !rows_ok(lse2) || !rows_ok(g))
+    return STREAMKL_ERR_INVALID;
+  if (want_dq && (!dq || !aligned16(dq))) return STREAMKL_ERR_INVALID;
+  if (setting == 2 && !rows_ok(kl)) return STREAMKL_ERR_INVALID;
+  if (bwd_mode == STREAMKL_BWD_AUTO) {
+    size_t l2 = 0;
+    if ((v = device_l2_bytes(&l2)) != STREAMKL_OK) return v;
+    bwd_mode = resolve_bwd_mode(p, bwd_mode, l2);
+  }
+  if (bwd_mode == STREAMKL_BWD_FUSED &&
+      (!workspace || !aligned16(workspace) || workspace_bytes < dq_acc_bytes(p)))
+    return STREAMKL_ERR_WORKSPACE;
+  int* status = nullptr;
+  if ((v = status_ptr(&status)) != STREAMKL_OK) return v;
+  BwdIn in{q1, k1, q2, k2, lse1, lse2, kl, g};
+  if (bwd_mode == STREAMKL_BWD_FUSED)
+    return from_cuda(launch_bwd_fused(p, setting, in, dq, dk, static_cast<float*>(workspace), status, st));
+  return from_cuda(launch_bwd_separate(p, setting, in, want_dq ? dq : nullptr, want_dk ? dk : nullptr, status, st));
+}
+
+streamkl_status streamkl_bwd_s1(const void* q1, const void* k1, const void* q2, const void* k2, streamkl_shape s,
+                                const float* lse1, const float* lse2, const float* g, void* dq2, void* dk2,
+                                int bwd_mode, void* workspace, size_t workspace_bytes, void* stream) {
+  return bwd_common(1, q1, k1, q2, k2, s, lse1, lse2, nullptr, g, dq2, dk2, bwd_mode, workspace, workspace_bytes,
+                    stream);
+}
+
+streamkl_status streamkl_bwd_s2(const void* q1, const void* k1, const void* q2, const void* k2, streamkl_shape s,
+                                const float* lse1, const float* lse2, const float* kl, const float* g, void* dq1,
+                                void* dk1, int bwd_mode, void* workspace, size_t workspace_bytes, void* stream) {
+  return bwd_common(2, q1, k1, q2, k2, s, lse1, lse2, kl, g, dq1, dk1, bwd_mode, workspace, workspace_bytes, stream);
+}
+
+streamkl_status streamkl_check_device_status(void* stream) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return STREAMKL_ERR_CUDA;
+  int h = 0;
+  if (cudaMemcpyFromSymbol(&h, g_streamkl_status, sizeof(int)) != cudaSuccess) return STREAMKL_ERR_CUDA;
+  const int zero = 0;
+  if (cudaMemcpyToSymbol(g_streamkl_status, &zero, sizeof(int)) != cudaSuccess) return STREAMKL_ERR_CUDA;
+  return (h & kStatusTimeout) ? STREAMKL_ERR_TIMEOUT : STREAMKL_OK;
+}
+
+streamkl_status streamkl_debug_wait_timeout(int timeout_us, void* stream) {
+  if (timeout_us < 1) timeout_us = 1;
+  if (timeout_us > 1000000) timeout_us = 1000000;
+  int* status = nullptr;
+  streamkl_status v = status_ptr(&status);
+  if (v != STREAMKL_OK) return v;
+  return from_cuda(launch_wait_timeout_probe(timeout_us, status, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,51 @@
+// Internal interface between the C-ABI layer (api.cu) and the kernel files.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace skl {
+
+// A validated problem.  Logits are handled in log2 units: c = scale * log2(e).
+struct Problem {
+  int B, H, NQ, NK, D;
+  int BH;
+  int causal;
+  int off;      // NK - NQ: row i keeps key j iff j <= i + off (causal)
+  float scale;  // softmax scale applied to Q K^T
+  float c;      // scale * log2(e)
+};
+
+// Builds a 3-D TMA map over a [BH, N, D] bf16 tensor with a {64, box_rows, 1}
+// box and the 128-byte swizzle.  Returns false if the driver rejects it.
+bool encode_tile_map(CUtensorMap* map, const void* base, int D, int N, int BH, int box_rows);
+
+// ---- forward (one CTA per 128-row query tile) -------------------------------
+cudaError_t launch_fwd(const Problem& p, const void* q1, const void* k1, const void* q2, const void* k2,
+                       float* kl, float* lse1, float* lse2, int* status, cudaStream_t st);
+
+// ---- Split-K forward ---------------------------------------------------------
+constexpr int kSplitKTile = 64;        // keys per pipeline stage
+constexpr int kSplitKCtasPerSm = 2;    // resident blocks per SM the planner assumes
+int splitk_key_tiles(const Problem& p);
+int splitk_plan(int BH, int key_tiles, int num_sms);
+cudaError_t launch_splitk(const Problem& p, const void* q1, const void* k1, const void* q2, const void* k2,
+                          int splits, float* partials, float* kl, float* lse1, float* lse2, int* status,
+                          cudaStream_t st);
+
+// ---- backward ------------------------------------------------------------------
+struct BwdIn {
+  const void *q1, *k1, *q2, *k2;
+  const float *lse1, *lse2, *kl, *g;
+};
+// setting 1: dq/dk are dQ2/dK2; setting 2: dQ1/dK1.  The separate path skips a NULL output.
+cudaError_t launch_bwd_separate(const Problem& p, int setting, const BwdIn& in, void* dq, void* dk, int* status,
+                                cudaStream_t st);
+cudaError_t launch_bwd_fused(const Problem& p, int setting, const BwdIn& in, void* dq, void* dk, float* dq_acc,
+                             int* status, cudaStream_t st);
+
+// ---- test hook ------------------------------------------------------------------
+cudaError_t launch_wait_timeout_probe(int timeout_us, int* status, cudaStream_t st);
+
+}  // namespace skl

@@ -1,0 +1,413 @@
+#!/usr/bin/env python
+"""Benchmark of the attention-KL hot path on one GB300 (or N independent ranks).
+
+Default workload: B=1, H=32, N_Q=N_K=65536, D=128, causal, bf16 inputs; one
+step is the forward (KL, LSE1, LSE2) plus the setting-1 backward (dQ2, dK2).
+Counted FLOPs are the MMA FLOPs on unmasked (query, key) pairs: 4D per pair for
+the forward and 8D per pair for the backward.
+
+Prints ONE JSON line (rank 0).  ``--impl reference`` times the fp64 CPU oracle
+instead, on bounded samples of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+# DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) of the
+# dominant kernel, from the ncu summary under profiles/ for the same kernel
+# build; None until measured or after the kernel changed.
+NCU_TRAFFIC_BYTES = {}
+
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return json.load(f), "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="kl_b1h32_n65536_d128_causal")
+    ap.add_argument("--setting", type=int, default=1, choices=[1, 2])
+    ap.add_argument("--bwd-mode", default="auto", choices=["auto", "fused", "separate"])
+    ap.add_argument("--nonsplit", action="store_true", help="decode workloads: time the non-split forward")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.hw_slowdown",
+              "clocks_event_reasons.hw_thermal_slowdown", "clocks_event_reasons.sw_thermal_slowdown",
+              "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu_id}", "--query-gpu=" + ",".join(self.FIELDS),
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) == len(self.FIELDS):
+                    rows.append(parts)
+        os.unlink(self.path)
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[0]) for r in rows if num(r[0]) is not None]
+        smax = [num(r[1]) for r in rows if num(r[1]) is not None]
+        pw = [num(r[2]) for r in rows if num(r[2]) is not None]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[3:]) if v.lower().startswith("active")})
+        # "under load": samples taken while the GPU draws well above idle
+        loaded = [s for s, p in zip(sm, pw) if p is not None and pw and p > 0.5 * max(pw)] or sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": reasons, "samples": len(rows)}
+
+
+def gpu_id_for(dev_index: int) -> str:
+    import torch
+    try:
+        u = str(torch.cuda.get_device_properties(dev_index).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+        if vis:
+            return vis.split(",")[dev_index]
+        return str(dev_index)
+
+
+# ----------------------------------------------------------------------------- oracle (CPU) sample
+
+def oracle_sample(w, setting: int, target_s: float):
+    """Times the fp64 oracle's forward + backward on the last R query rows of head (0, 0).
+
+    Returns (counted TFLOP/s, seconds, rows, description)."""
+    from attention_kl_divergence_streamkl_gb300 import synth
+    from oracle import oracle as O
+    q1, k1, q2, k2 = (synth.bf16_bits_to_f64(synth.head_slice(w, k, 0, 0)) for k in ("q1", "k1", "q2", "k2"))
+    g = synth.upstream_grad(w)[0, 0].astype(np.float64)
+
+    def run(rows):
+        t0 = time.perf_counter()
+        O.rows_forward(q1, k1, q2, k2, w.softmax_scale, w.causal, rows)
+        O.head_backward_rows(setting, q1, k1, q2, k2, w.softmax_scale, w.causal, g, rows)
+        return time.perf_counter() - t0
+
+    def pairs(rows):
+        if not w.causal:
+            return rows.size * w.NK
+        return int(np.minimum(w.NK, rows + (w.NK - w.NQ) + 1).sum())
+
+    probe = np.arange(max(0, w.NQ - 16), w.NQ)
+    dt = run(probe)
+    R = int(min(w.NQ, max(16, probe.size * target_s / max(dt, 1e-6))))
+    rows = np.arange(w.NQ - R, w.NQ)
+    dt = run(rows)
+    flops = 12 * w.D * pairs(rows)
+    desc = (f"fp64 oracle forward + setting-{setting} backward on the last {R} query rows of head (0,0) "
+            f"({pairs(rows)} unmasked pairs, {flops:.3e} counted FLOP)")
+    return flops / dt / 1e12, dt, R, desc
+
+
+def cpu_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+# ----------------------------------------------------------------------------- reference arm
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    from attention_kl_divergence_streamkl_gb300 import synth
+    from oracle import oracle as O
+    w = synth.WORKLOADS[args.workload]
+    decode = w.name.startswith("decode")
+    q1, k1, q2, k2 = (synth.bf16_bits_to_f64(synth.head_slice(w, k, 0, 0)) for k in ("q1", "k1", "q2", "k2"))
+    g = synth.upstream_grad(w)[0, 0].astype(np.float64)
+    # rows per step: sized so that one step is ~ a couple of seconds of CPU work
+    R = 64 if not decode else w.NQ
+    rows = np.arange(w.NQ - R, w.NQ)
+    pairs = int(np.minimum(w.NK, rows + (w.NK - w.NQ) + 1).sum()) if w.causal else rows.size * w.NK
+
+    def step():
+        O.rows_forward(q1, k1, q2, k2, w.softmax_scale, w.causal, rows)
+        if not decode:
+            O.head_backward_rows(args.setting, q1, k1, q2, k2, w.softmax_scale, w.causal, g, rows)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t0
+    sample = f"fp64 oracle on the last {R} query rows of head (0,0) of {w.name} per step ({pairs} pairs)"
+    if decode:
+        nbytes = 2 * w.NK * w.D * 2
+        value = args.steps * nbytes / dt / 1e9
+        metric, unit = "attn-KL split-K decode fwd GB/s (B8 H32 N_K=131072 D128)", "GB/s"
+    else:
+        value = args.steps * 12 * w.D * pairs / dt / 1e12
+        metric, unit = "attn-KL fwd+bwd TFLOP/s & ms (H32 D128 N64K causal), % bf16 TC peak", "TFLOP/s"
+    line = {"impl": "reference", "metric": metric, "value": value, "unit": unit, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": w.name, "sample_rows": R},
+            "cpu_baseline": {"value": value, "unit": unit, "cores": cpu_cores(), "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+# ----------------------------------------------------------------------------- our arm
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    from attention_kl_divergence_streamkl_gb300 import build as B
+    B.build()
+    import attention_kl_divergence_streamkl_gb300 as skl
+    from attention_kl_divergence_streamkl_gb300 import synth
+
+    w = synth.WORKLOADS[args.workload]
+    decode = w.name.startswith("decode")
+    mode = {"auto": skl.BWD_AUTO, "fused": skl.BWD_FUSED, "separate": skl.BWD_SEPARATE}[args.bwd_mode]
+    if not decode and mode == skl.BWD_AUTO:
+        mode = skl.bwd_select(w.B, w.H, w.NQ, w.NK, w.D, torch.cuda.get_device_properties(dev).L2_cache_size,
+                              w.causal)
+    inp = synth.make_inputs(w)
+    host = [torch.from_numpy(inp[k].view(np.int16)).view(torch.bfloat16) for k in ("q1", "k1", "q2", "k2")]
+    host_g = torch.from_numpy(inp["g"])
+    q1, k1, q2, k2 = (t.to(dev) for t in host)
+    g = host_g.to(dev)
+    scale, causal = w.softmax_scale, w.causal
+    pairs = w.unmasked_pairs()
+    stream = torch.cuda.current_stream(dev)
+
+    # ---- one step, with an event between kernels so each is timed on its stream
+    def step(qs, ev=None):
+        a, b, c, d = qs
+        if decode:
+            out = skl.fwd(a, b, c, d, scale, causal) if args.nonsplit else skl.fwd_splitk(a, b, c, d, scale, causal)
+            if ev:
+                ev[1].record(stream)
+            return out
+        kl, l1, l2 = skl.fwd(a, b, c, d, scale, causal)
+        if ev:
+            ev[1].record(stream)
+        bwd = skl.bwd_s1 if args.setting == 1 else skl.bwd_s2
+        extra = () if args.setting == 1 else (kl,)
+        if mode == skl.BWD_SEPARATE:
+            dq = bwd(a, b, c, d, l1, l2, *extra, g, scale, causal, skl.BWD_DQ_ONLY)[0]
+            if ev:
+                ev[2].record(stream)
+            dk = bwd(a, b, c, d, l1, l2, *extra, g, scale, causal, skl.BWD_DK_ONLY)[1]
+        else:
+            dq, dk = bwd(a, b, c, d, l1, l2, *extra, g, scale, causal, mode)
+            if ev:
+                ev[2].record(stream)
+        if ev:
+            ev[3].record(stream)
+        return kl, dq, dk
+
+    if decode:
+        kernels = ["fwd" if args.nonsplit else "splitk"]
+        algo = {kernels[0]: 4 * w.D * pairs}
+        launches_per_step = 1 if args.nonsplit else 2
+    elif mode == skl.BWD_SEPARATE:
+        kernels = ["fwd", "bwd_dq", "bwd_dk"]
+        algo = {"fwd": 4 * w.D * pairs, "bwd_dq": 6 * w.D * pairs, "bwd_dk": 6 * w.D * pairs}
+        launches_per_step = 3
+    else:
+        kernels = ["fwd", "bwd_fused", "none"]
+        algo = {"fwd": 4 * w.D * pairs, "bwd_fused": 8 * w.D * pairs}
+        launches_per_step = 3
+
+    for _ in range(args.warmup):
+        step((q1, k1, q2, k2))
+    torch.cuda.synchronize(dev)
+    assert skl.check_device_status(dev) == 0, "device-side timeout during warm-up"
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(gpu_id_for(local))
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    sampler.start()
+    t_start.record(stream)
+    for i in range(args.steps):
+        evs[i][0].record(stream)
+        step((q1, k1, q2, k2), evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+    if world > 1:
+        dist.barrier()
+    elapsed_ms = t_start.elapsed_time(t_end)
+    per_kernel = {k: 0.0 for k in kernels}
+    for e in evs:
+        per_kernel[kernels[0]] += e[0].elapsed_time(e[1])
+        if len(kernels) > 1:
+            per_kernel[kernels[1]] += e[1].elapsed_time(e[2])
+            per_kernel[kernels[2]] += e[2].elapsed_time(e[3])
+    per_kernel.pop("none", None)
+    status = skl.check_device_status(dev)
+    assert status == 0, f"device-side timeout in the timed region (status {status})"
+
+    if world > 1:
+        t = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+
+    peaks, peak_src = load_peaks()
+    ms_step = elapsed_ms / args.steps
+    if decode:
+        bytes_step = 2 * w.B * w.H * w.NK * w.D * 2 + 2 * w.B * w.H * w.NQ * w.D * 2
+        value = world * bytes_step / (ms_step / 1e3) / 1e9
+        metric, unit = "attn-KL split-K decode fwd GB/s (B8 H32 N_K=131072 D128)", "GB/s"
+        dom = kernels[0]
+        achieved = bytes_step / (per_kernel[dom] / args.steps / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"], "traffic": NCU_TRAFFIC_BYTES.get(dom), "kernel": dom,
+                "peak_source": f"{peak_src} hbm_gbs", "algorithmic_bytes_per_launch": bytes_step}
+    else:
+        flops_step = 12 * w.D * pairs
+        value = world * flops_step / (ms_step / 1e3) / 1e12
+        metric, unit = "attn-KL fwd+bwd TFLOP/s & ms (H32 D128 N64K causal), % bf16 TC peak", "TFLOP/s"
+        dom = max(per_kernel, key=per_kernel.get)
+        avg_ms = per_kernel[dom] / args.steps
+        achieved = algo[dom] / (avg_ms / 1e3) / 1e12
+        peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                "traffic": NCU_TRAFFIC_BYTES.get(dom), "kernel": dom,
+                "peak_source": f"{peak_src} bf16_tflops_sustained (kernel timed inside a long step)",
+                "algorithmic_flops_per_launch": algo[dom],
+                "frac_of_burst_peak_whole_step": value / world / peaks["bf16_tflops"]}
+
+    # ---- end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        pinned = [t.pin_memory() for t in host]
+        pg = host_g.pin_memory()
+        out_host = torch.empty((w.B, w.H, w.NQ), dtype=torch.float32).pin_memory()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        for _ in range(args.steps):
+            dqs = [t.to(dev, non_blocking=True) for t in pinned]
+            if not decode:
+                g.copy_(pg, non_blocking=True)  # the upstream gradient is a host input too
+            kl = step(dqs)[0]
+            out_host.copy_(kl, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = e0.elapsed_time(e1) / args.steps
+        h2d = sum(t.numel() * t.element_size() for t in pinned) + (0 if decode else pg.numel() * 4)
+        d2h = out_host.numel() * 4
+        work = (bytes_step if decode else flops_step)
+        e2e = {"value": world * work / (e2e_ms / 1e3) / (1e9 if decode else 1e12), "unit": unit,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        if decode:
+            cpu = None
+        else:
+            v, dt, R, desc = oracle_sample(w, args.setting, args.cpu_seconds)
+            cpu = {"value": v, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle", "sample": desc,
+                   "seconds": dt}
+
+    line = {"metric": metric, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "N_Q": w.NQ, "N_K": w.NK, "D": w.D,
+                       "causal": w.causal, "setting": args.setting if not decode else None,
+                       "bwd_path": None if decode else {1: "fused", 2: "separate"}[mode],
+                       "path": ("nonsplit" if args.nonsplit else "splitk") if decode else "fwd+bwd",
+                       "per_gpu_units": "the whole workload on every rank (independent heads)",
+                       "l2": "inputs larger than L2, no flush between steps",
+                       "parallelism": f"replicas{world}"},
+            "roofline": roof, "per_kernel_ms": {k: v / args.steps for k, v in per_kernel.items()},
+            "gpu_launches": launches_per_step * args.steps, "clocks": clocks, "e2e": e2e, "cpu_baseline": cpu}
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

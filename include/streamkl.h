@@ -1,0 +1,160 @@
+/*
+ * libstreamkl — fused attention KL divergence for one GB300 GPU (sm_103a).
+ *
+ * For every (batch b, head h, query row i) the library computes
+ *
+ *     S_t = scale * Q_t K_t^T,  P_t = row-softmax(S_t)   (t = 1 teacher, t = 2 student)
+ *     KL_i = sum_j P1_ij (log P1_ij - log P2_ij)           i.e. KL(P1 || P2)
+ *     LSE_t,i = log sum_j exp(S_t,ij)
+ *
+ * over the keys j that the (optional) causal mask keeps, without ever writing
+ * an N_Q x N_K matrix to memory.  The forward is the one-pass online
+ * formulation with five running scalars per row (m1, m2, l1, l2, acc) and the
+ * closing identity KL = acc/l1 + LSE2 - LSE1 (StreamKL technical summary,
+ * gist.science/ja/paper/2606.20005, section 手法 1 "online formulation").  The
+ * backward rebuilds P_t = exp(S_t - LSE_t) tile by tile from Q, K and the saved
+ * LSE (section 手法 2 "recompute strategy") in the two settings named there.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Q_t are [B, H, N_Q, D] and K_t are [B, H, N_K, D], bf16, contiguous,
+ *   DEVICE pointers, 16-byte aligned.  D is 64 or 128.
+ * - Row outputs and inputs (KL, LSE1, LSE2, g) are fp32 [B, H, N_Q], device.
+ * - Gradient outputs are bf16 in the layout of the tensor they belong to.
+ * - scale <= 0 selects 1/sqrt(D).  causal != 0 keeps key j for row i iff
+ *   j <= i + N_K - N_Q (bottom-right alignment); causal with N_Q > N_K is
+ *   rejected so that no row is left without keys.
+ * - The caller owns every buffer; the library allocates no device memory.
+ *   Scratch memory is passed in as a workspace whose size is queried first.
+ * - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls are
+ *   asynchronous on it.  Argument errors are returned synchronously before
+ *   anything is launched.  Launch failures return STREAMKL_ERR_CUDA.
+ * - Device-side waits are bounded.  A wait that runs out sets a device status
+ *   word instead of hanging; streamkl_check_device_status() reads it.
+ * - No C++ exception crosses this interface.
+ */
+#ifndef STREAMKL_H
+#define STREAMKL_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  STREAMKL_OK = 0,
+  STREAMKL_ERR_INVALID = 1,     /* bad shape, null/misaligned pointer, causal with N_Q > N_K */
+  STREAMKL_ERR_UNSUPPORTED = 2, /* valid but not handled (e.g. D not in {64,128}, Split-K N_Q > 16) */
+  STREAMKL_ERR_WORKSPACE = 3,   /* workspace pointer missing, misaligned or too small */
+  STREAMKL_ERR_CUDA = 4,        /* a CUDA runtime/driver call failed (launch, memset, tensor map) */
+  STREAMKL_ERR_TIMEOUT = 5      /* a bounded device-side wait ran out (reported by check_device_status) */
+} streamkl_status;
+
+/* Problem shape.  scale <= 0 means 1/sqrt(D). */
+typedef struct {
+  int B, H, NQ, NK, D;
+  float scale;
+  int causal;
+} streamkl_shape;
+
+/* Backward path selection (the adaptive rule of section 手法 2 "kernel fusion"). */
+typedef enum {
+  STREAMKL_BWD_AUTO = 0,     /* fused when the fp32 dQ buffer fits in L2, else separate */
+  STREAMKL_BWD_FUSED = 1,    /* one pass over each QK tile pair, dQ by atomics into fp32 */
+  STREAMKL_BWD_SEPARATE = 2, /* a Q-stationary dQ kernel and a K-stationary dK kernel */
+  STREAMKL_BWD_DQ_ONLY = 3,  /* separate path, dQ kernel only (dK pointer may be NULL) */
+  STREAMKL_BWD_DK_ONLY = 4   /* separate path, dK kernel only (dQ pointer may be NULL) */
+} streamkl_bwd_mode;
+
+/* Largest N_Q the Split-K forward takes. */
+#define STREAMKL_SPLITK_MAX_NQ 16
+
+/*
+ * Forward: KL, LSE1, LSE2 [B,H,N_Q] fp32 from bf16 Q1, K1, Q2, K2.
+ * (technical summary, 手法 1 "online formulation": five running scalars,
+ *  KL = acc/l1 + LSE2 - LSE1, whole key tiles past the causal boundary skipped.)
+ * One CTA owns a tile of query rows and streams every key tile it needs.
+ */
+streamkl_status streamkl_fwd(const void* q1, const void* k1, const void* q2, const void* k2,
+                             streamkl_shape s, float* kl, float* lse1, float* lse2, void* stream);
+
+/*
+ * Split-K forward for few query rows (decode, N_Q <= STREAMKL_SPLITK_MAX_NQ).
+ * (technical summary, 手法 3 "Split-K variant": the key dimension is divided
+ *  over thread blocks so that a small N_Q still fills the SMs.)
+ * Each of `num_splits` blocks per (b, h) reduces a contiguous key range to the
+ * five partial scalars per row; a second kernel merges them.  num_splits = 0
+ * picks a count that fills the GPU.  Workspace: fp32 [B,H,N_Q,splits,5], size
+ * from streamkl_fwd_splitk_workspace(), 16-byte aligned, contents ignored.
+ */
+streamkl_status streamkl_fwd_splitk_workspace(streamkl_shape s, int num_splits, size_t* bytes);
+streamkl_status streamkl_fwd_splitk(const void* q1, const void* k1, const void* q2, const void* k2,
+                                    streamkl_shape s, int num_splits, void* workspace,
+                                    size_t workspace_bytes, float* kl, float* lse1, float* lse2,
+                                    void* stream);
+/*
+ * The split count num_splits = 0 resolves to, for a GPU with `num_sms` SMs
+ * (num_sms <= 0: the current device).  It minimises waves x (tiles per block
+ * + a fixed per-block cost); with num_sms > 0 it is a pure host computation.
+ */
+streamkl_status streamkl_fwd_splitk_plan(streamkl_shape s, int num_sms, int* num_splits);
+
+/*
+ * Backward workspace: fused mode needs an fp32 [B,H,N_Q,D] dQ accumulator
+ * (zeroed by the library); separate mode needs none (0 bytes).  AUTO resolves
+ * with the current device's L2 size.
+ */
+streamkl_status streamkl_bwd_workspace(streamkl_shape s, int bwd_mode, size_t* bytes);
+/* Which path AUTO takes for a device with `l2_bytes` of L2 (pure host rule, no device). */
+int streamkl_bwd_select(streamkl_shape s, size_t l2_bytes);
+
+/*
+ * Setting 1: P1 held fixed, Q2/K2 optimised (standard distillation).
+ * (technical summary, 手法 2 "recompute strategy", setting 1.)
+ * Rebuilds P_t = exp(S_t - LSE_t); dS2 = g_i (P2 - P1); writes
+ * dQ2 = scale dS2 K2 and dK2 = scale dS2^T Q2 (bf16).  g is dLoss/dKL_i, fp32
+ * [B,H,N_Q] (a mean over rows is g = 1/N_Q).  lse1/lse2 are the forward's.
+ */
+streamkl_status streamkl_bwd_s1(const void* q1, const void* k1, const void* q2, const void* k2,
+                                streamkl_shape s, const float* lse1, const float* lse2,
+                                const float* g, void* dq2, void* dk2, int bwd_mode,
+                                void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Setting 2: P2 held fixed, Q1/K1 optimised.
+ * (technical summary, 手法 2, setting 2; 手法 3 "numerical stability": the log
+ *  ratio comes from logits and stored LSEs, never from log of probabilities.)
+ * r = (S1 - LSE1) - (S2 - LSE2); dS1 = g_i P1 (r - KL_i); writes
+ * dQ1 = scale dS1 K1 and dK1 = scale dS1^T Q1 (bf16).  kl is the forward's.
+ */
+streamkl_status streamkl_bwd_s2(const void* q1, const void* k1, const void* q2, const void* k2,
+                                streamkl_shape s, const float* lse1, const float* lse2,
+                                const float* kl, const float* g, void* dq1, void* dk1, int bwd_mode,
+                                void* workspace, size_t workspace_bytes, void* stream);
+
+/* Text for a status code (static storage). */
+const char* streamkl_status_string(streamkl_status st);
+
+/*
+ * Synchronises `stream`, then reads and clears the device status word of the
+ * current device.  Returns STREAMKL_ERR_TIMEOUT if a bounded wait ran out since
+ * the last check, STREAMKL_ERR_CUDA if the sync failed, else STREAMKL_OK.
+ */
+streamkl_status streamkl_check_device_status(void* stream);
+
+/*
+ * Test hook for the timeout path: launches one block that waits on a barrier
+ * nobody arrives at, giving up after `timeout_us` microseconds (clamped to
+ * [1, 1000000]) and recording STREAMKL_ERR_TIMEOUT in the status word.
+ */
+streamkl_status streamkl_debug_wait_timeout(int timeout_us, void* stream);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int streamkl_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* STREAMKL_H */

@@ -43,8 +43,8 @@ from __future__ import annotations
 import numpy as np
 
 __all__ = [
-    "logits", "causal_mask", "row_softmax", "kl_from_probs", "head_forward",
-    "head_backward", "forward", "backward", "rows_forward", "rows_backward_dq",
+    "logits", "causal_mask", "row_softmax", "kl_from_probs", "head_forward", "dlogits",
+    "head_backward_rows", "head_backward", "forward", "backward", "rows_forward", "rows_backward_dq",
     "materialised_distribution_bytes",
 ]
 
@@ -97,7 +97,7 @@ def _key_limit(rows: np.ndarray, nq: int, nk: int, causal: bool) -> int:
     """Keys past the last row's causal frontier have P = 0 exactly; leave them out."""
     if not causal:
         return nk
-    return int(min(nk, rows[-1] + (nk - nq) + 1))
+    return int(min(nk, rows.max() + (nk - nq) + 1))
 
 
 def _rows_state(q1, k1, q2, k2, scale, causal, rows):
@@ -136,19 +136,32 @@ def dlogits(setting: int, P1: np.ndarray, P2: np.ndarray, kl: np.ndarray, g: np.
     raise ValueError("setting must be 1 or 2")
 
 
+def head_backward_rows(setting: int, q1, k1, q2, k2, scale: float, causal: bool, g, rows):
+    """dQ_t of the given query rows and their contribution to dK_t (one head).
+
+    dK_t = scale sum_i dS_i^T q_i is a sum over query rows, so the full dK_t is
+    the sum of these contributions over any partition of the rows.
+    """
+    rows = np.asarray(rows, dtype=np.int64)
+    q_opt, k_opt = (q2, k2) if setting == 1 else (q1, k1)
+    dk = np.zeros((k1.shape[0], q1.shape[1]))
+    P1, P2, kl, _, _, kmax = _rows_state(q1, k1, q2, k2, scale, causal, rows)
+    dS = dlogits(setting, P1, P2, kl, np.asarray(g, np.float64)[rows])
+    dq = scale * (dS @ np.asarray(k_opt[:kmax], np.float64))
+    dk[:kmax] = scale * (dS.T @ np.asarray(q_opt[rows], np.float64))
+    return dq, dk
+
+
 def head_backward(setting: int, q1, k1, q2, k2, scale: float, causal: bool, g,
                   block: int = ROW_BLOCK):
     """(dQ_t, dK_t) of one head for the optimised pair t (2 in setting 1, 1 in setting 2)."""
     nq, nk, d = q1.shape[0], k1.shape[0], q1.shape[1]
-    q_opt, k_opt = (q2, k2) if setting == 1 else (q1, k1)
     dq = np.zeros((nq, d))
     dk = np.zeros((nk, d))
-    g = np.asarray(g, np.float64)
     for rows in _block_rows(nq, block):
-        P1, P2, kl, _, _, kmax = _rows_state(q1, k1, q2, k2, scale, causal, rows)
-        dS = dlogits(setting, P1, P2, kl, g[rows])
-        dq[rows] = scale * (dS @ np.asarray(k_opt[:kmax], np.float64))
-        dk[:kmax] += scale * (dS.T @ np.asarray(q_opt[rows], np.float64))
+        dq_r, dk_r = head_backward_rows(setting, q1, k1, q2, k2, scale, causal, g, rows)
+        dq[rows] = dq_r
+        dk += dk_r
     return dq, dk
 
 
@@ -177,29 +190,33 @@ def backward(setting: int, Q1, K1, Q2, K2, scale: float, causal: bool, g, block:
     return dq, dk
 
 
-def rows_forward(q1, k1, q2, k2, scale: float, causal: bool, rows):
-    """KL, LSE1, LSE2 of selected query rows of one head; O(N_K D) per row."""
+def rows_forward(q1, k1, q2, k2, scale: float, causal: bool, rows, block: int = ROW_BLOCK):
+    """KL, LSE1, LSE2 of selected query rows (any order) of one head; O(N_K D) per row."""
     rows = np.asarray(rows, dtype=np.int64)
     out = [np.empty(rows.size) for _ in range(3)]
-    for n, r in enumerate(rows):
-        _, _, kl, l1, l2, _ = _rows_state(q1, k1, q2, k2, scale, causal, np.array([r]))
-        out[0][n], out[1][n], out[2][n] = kl[0], l1[0], l2[0]
+    for b0 in range(0, rows.size, block):
+        sel = rows[b0:b0 + block]
+        _, _, kl, l1, l2, _ = _rows_state(q1, k1, q2, k2, scale, causal, sel)
+        out[0][b0:b0 + sel.size], out[1][b0:b0 + sel.size], out[2][b0:b0 + sel.size] = kl, l1, l2
     return tuple(out)
 
 
-def rows_backward_dq(setting: int, q1, k1, q2, k2, scale: float, causal: bool, g_rows, rows):
+def rows_backward_dq(setting: int, q1, k1, q2, k2, scale: float, causal: bool, g_rows, rows,
+                     block: int = ROW_BLOCK):
     """dQ rows [len(rows), D] of the optimised pair for selected query rows of one head.
 
     A query row's gradient depends only on its own row of S1 and S2, so it is
-    exact to evaluate it alone.
+    exact to evaluate rows apart from the rest.
     """
     rows = np.asarray(rows, dtype=np.int64)
+    g_rows = np.asarray(g_rows, np.float64)
     k_opt = k2 if setting == 1 else k1
     out = np.empty((rows.size, q1.shape[1]))
-    for n, r in enumerate(rows):
-        P1, P2, kl, _, _, kmax = _rows_state(q1, k1, q2, k2, scale, causal, np.array([r]))
-        dS = dlogits(setting, P1, P2, kl, np.array([g_rows[n]], np.float64))
-        out[n] = scale * (dS @ np.asarray(k_opt[:kmax], np.float64))[0]
+    for b0 in range(0, rows.size, block):
+        sel = rows[b0:b0 + block]
+        P1, P2, kl, _, _, kmax = _rows_state(q1, k1, q2, k2, scale, causal, sel)
+        dS = dlogits(setting, P1, P2, kl, g_rows[b0:b0 + sel.size])
+        out[b0:b0 + sel.size] = scale * (dS @ np.asarray(k_opt[:kmax], np.float64))
     return out
 
 

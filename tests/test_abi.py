@@ -1,0 +1,161 @@
+"""The C-ABI library: it loads, exports what include/streamkl.h declares, and its
+host-side rules (validation, Split-K planning, backward path choice, workspace
+sizes) behave as documented.  Nothing here launches a kernel."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from attention_kl_divergence_streamkl_gb300 import _lib as K
+from attention_kl_divergence_streamkl_gb300 import build as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "streamkl.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return K.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(streamkl_\w+)\s*\(", text)))
+
+
+def test_header_and_binding_agree():
+    assert declared_functions() == sorted(K.SIGNATURES)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    assert lib.streamkl_version() >= 100
+
+
+def test_status_strings(lib):
+    for code in range(6):
+        assert K.status_string(code)
+    assert "timed out" in K.status_string(K.ERR_TIMEOUT)
+
+
+def fake_ptr(off=0):
+    return ctypes.c_void_p(0x10000000 + off)
+
+
+def call_fwd(lib, shape, q=None, kl=None):
+    q = q or fake_ptr()
+    kl = kl or fake_ptr(4096)
+    return lib.streamkl_fwd(q, fake_ptr(64), fake_ptr(128), fake_ptr(192), shape, kl, fake_ptr(8192),
+                            fake_ptr(12288), None)
+
+
+@pytest.mark.parametrize("shape,code", [
+    (dict(B=0, H=1, NQ=8, NK=8, D=64), K.ERR_INVALID),
+    (dict(B=1, H=0, NQ=8, NK=8, D=64), K.ERR_INVALID),
+    (dict(B=1, H=1, NQ=-1, NK=8, D=64), K.ERR_INVALID),
+    (dict(B=1, H=1, NQ=8, NK=0, D=64), K.ERR_INVALID),
+    (dict(B=1, H=1, NQ=8, NK=8, D=96), K.ERR_UNSUPPORTED),
+    (dict(B=1, H=1, NQ=8, NK=8, D=256), K.ERR_UNSUPPORTED),
+    (dict(B=1, H=1, NQ=9, NK=8, D=64, causal=True), K.ERR_INVALID),
+    (dict(B=1, H=1, NQ=8, NK=8, D=64, scale=float("nan")), K.ERR_INVALID),
+    (dict(B=1, H=1, NQ=8, NK=8, D=64, scale=float("inf")), K.ERR_INVALID),
+    (dict(B=1, H=1, NQ=8, NK=2**31 - 1, D=64), K.ERR_UNSUPPORTED),
+    (dict(B=65536, H=65536, NQ=8, NK=8, D=64), K.ERR_UNSUPPORTED),
+])
+def test_fwd_rejects_bad_shapes_before_launch(lib, shape, code):
+    assert call_fwd(lib, K.make_shape(**shape)) == code
+
+
+def test_fwd_rejects_null_and_misaligned_pointers(lib):
+    s = K.make_shape(1, 1, 8, 8, 64)
+    assert lib.streamkl_fwd(None, fake_ptr(), fake_ptr(), fake_ptr(), s, fake_ptr(), fake_ptr(), fake_ptr(),
+                            None) == K.ERR_INVALID
+    assert call_fwd(lib, s, q=fake_ptr(8)) == K.ERR_INVALID  # Q not 16-byte aligned
+    assert call_fwd(lib, s, kl=fake_ptr(2)) == K.ERR_INVALID  # fp32 output not 4-byte aligned
+
+
+def test_empty_query_set_is_a_no_op(lib):
+    # N_Q = 0: nothing to compute, no pointer is touched
+    s = K.make_shape(2, 3, 0, 16, 128)
+    assert lib.streamkl_fwd(None, None, None, None, s, None, None, None, None) == K.OK
+
+
+def test_bwd_rejects_bad_mode_and_pointers(lib):
+    s = K.make_shape(1, 1, 8, 8, 64)
+    p = [fake_ptr(64 * i) for i in range(12)]
+    assert lib.streamkl_bwd_s1(p[0], p[1], p[2], p[3], s, p[4], p[5], p[6], p[7], p[8], 7, None, 0,
+                               None) == K.ERR_INVALID
+    assert lib.streamkl_bwd_s2(p[0], p[1], p[2], p[3], s, p[4], p[5], None, p[6], p[7], p[8], K.BWD_SEPARATE,
+                               None, 0, None) == K.ERR_INVALID  # setting 2 needs the saved KL
+    assert lib.streamkl_bwd_s1(p[0], p[1], p[2], p[3], s, p[4], p[5], p[6], p[7], fake_ptr(2), K.BWD_SEPARATE,
+                               None, 0, None) == K.ERR_INVALID  # dK misaligned
+    # fused without (enough) workspace is refused before any launch
+    assert lib.streamkl_bwd_s1(p[0], p[1], p[2], p[3], s, p[4], p[5], p[6], p[7], p[8], K.BWD_FUSED, None, 0,
+                               None) == K.ERR_WORKSPACE
+    assert lib.streamkl_bwd_s1(p[0], p[1], p[2], p[3], s, p[4], p[5], p[6], p[7], p[8], K.BWD_FUSED, p[9],
+                               8 * 64 * 4 - 1, None) == K.ERR_WORKSPACE
+
+
+def test_workspace_sizes(lib):
+    n = ctypes.c_size_t()
+    s = K.make_shape(8, 32, 4, 131072, 128)
+    assert lib.streamkl_fwd_splitk_workspace(s, 19, ctypes.byref(n)) == K.OK
+    assert n.value == 8 * 32 * 4 * 19 * 5 * 4
+    s16 = K.make_shape(8, 32, 17, 131072, 128)
+    assert lib.streamkl_fwd_splitk_workspace(s16, 19, ctypes.byref(n)) == K.ERR_UNSUPPORTED
+    s = K.make_shape(2, 32, 4096, 4096, 128)
+    assert lib.streamkl_bwd_workspace(s, K.BWD_FUSED, ctypes.byref(n)) == K.OK
+    assert n.value == 2 * 32 * 4096 * 128 * 4
+    assert lib.streamkl_bwd_workspace(s, K.BWD_SEPARATE, ctypes.byref(n)) == K.OK
+    assert n.value == 0
+    for mode in (K.BWD_DQ_ONLY, K.BWD_DK_ONLY):
+        assert lib.streamkl_bwd_workspace(s, mode, ctypes.byref(n)) == K.OK
+        assert n.value == 0
+    assert lib.streamkl_bwd_workspace(s, 5, ctypes.byref(n)) == K.ERR_INVALID
+
+
+def test_splitk_workspace_rejects_bad_split_counts(lib):
+    p = [fake_ptr(64 * i) for i in range(8)]
+    s = K.make_shape(1, 2, 3, 1000, 64)
+    assert lib.streamkl_fwd_splitk(p[0], p[1], p[2], p[3], s, -1, p[4], 1 << 20, p[5], p[6], p[7],
+                                   None) == K.ERR_INVALID
+    assert lib.streamkl_fwd_splitk(p[0], p[1], p[2], p[3], s, 4, p[4], 2 * 3 * 4 * 20 - 1, p[5], p[6], p[7],
+                                   None) == K.ERR_WORKSPACE
+    assert lib.streamkl_fwd_splitk(p[0], p[1], p[2], p[3], s, 4, fake_ptr(8), 1 << 20, p[5], p[6], p[7],
+                                   None) == K.ERR_WORKSPACE  # misaligned workspace
+
+
+def _cost(bh, tiles, sms, s):
+    slots = sms * 2
+    waves = -(-bh * s // slots)
+    return waves * (-(-tiles // s) + 2)
+
+
+@pytest.mark.parametrize("bh,nk,sms", [(256, 131072, 152), (32, 4096, 152), (1, 100, 152), (7, 65536, 132),
+                                       (1024, 64, 152)])
+def test_splitk_plan_minimises_the_wave_model(lib, bh, nk, sms):
+    s = K.splitk_plan(1, bh, 4, nk, 128, num_sms=sms)
+    tiles = -(-nk // 64)
+    assert 1 <= s <= tiles
+    best = min(_cost(bh, tiles, sms, x) for x in range(1, min(tiles, 4096) + 1))
+    assert _cost(bh, tiles, sms, s) == best
+    ideal = bh * tiles / (sms * 2)
+    if ideal >= 100:
+        # with many tiles per slot the chosen split keeps the SMs >90% busy under the model
+        assert ideal / _cost(bh, tiles, sms, s) > 0.9
+
+
+def test_bwd_select_rule(lib):
+    # fused exactly while the fp32 dQ buffer [B,H,N_Q,D] fits in L2
+    l2 = 126 * 2**20
+    assert K.bwd_select(1, 1, 128, 128, 64, l2) == K.BWD_FUSED
+    fits = 126 * 2**20 // (32 * 128 * 4)
+    assert K.bwd_select(1, 32, fits, fits, 128, l2) == K.BWD_FUSED
+    assert K.bwd_select(1, 32, fits + 1, fits + 1, 128, l2) == K.BWD_SEPARATE
+    assert K.bwd_select(2, 32, 4096, 4096, 128, l2) == K.BWD_SEPARATE  # 128 MiB > 126 MiB
+    assert K.bwd_select(1, 32, 65536, 65536, 128, l2) == K.BWD_SEPARATE
+    assert K.bwd_select(0, 1, 8, 8, 64, l2) == 0  # invalid shape

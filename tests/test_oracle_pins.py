@@ -174,3 +174,19 @@ def _mut_transposed_dk(mp):
 def test_planted_mistake_is_caught(monkeypatch, mutation):
     mutation(monkeypatch)
     assert _run_all(), "a planted mistake passed every pin"
+
+
+def test_row_subsets_agree_with_full_head():
+    """The sampled-row entry points give the full-head values for any row order."""
+    rng = np.random.default_rng(5)
+    for nq, nk, causal in ((40, 40, True), (23, 61, True), (31, 17, False)):
+        q1, k1, q2, k2 = (rng.standard_normal((n, 8)) for n in (nq, nk, nq, nk))
+        g = rng.uniform(0.5, 1.5, nq)
+        kl, l1, l2 = O.head_forward(q1, k1, q2, k2, 0.4, causal)
+        rows = rng.permutation(nq)[: nq // 2]
+        a, b, c = O.rows_forward(q1, k1, q2, k2, 0.4, causal, rows, block=5)
+        assert np.allclose(a, kl[rows], atol=1e-13) and np.allclose(b, l1[rows]) and np.allclose(c, l2[rows])
+        for setting in (1, 2):
+            dq, _ = O.head_backward(setting, q1, k1, q2, k2, 0.4, causal, g)
+            got = O.rows_backward_dq(setting, q1, k1, q2, k2, 0.4, causal, g[rows], rows, block=4)
+            assert np.allclose(got, dq[rows], atol=1e-13)
