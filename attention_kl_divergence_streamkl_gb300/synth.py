@@ -164,7 +164,7 @@ def make_inputs(w: Workload, threads: int | None = None) -> dict[str, np.ndarray
 
 def upstream_grad(w: Workload) -> np.ndarray:
     """Per-row dLoss/dKL_i for a mean over query rows: the constant 1/N_Q."""
-    return np.full((w.B, w.H, w.NQ), 1.0 / w.NQ, dtype=np.float32)
+    return np.full((w.B, w.H, w.NQ), 1.0 / max(w.NQ, 1), dtype=np.float32)
 
 
 def sample_rows(w: Workload, count: int, seed: int) -> np.ndarray:

@@ -55,8 +55,17 @@ def rel_fro(got, ref) -> float:
     return float(np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-300))
 
 
+# Where the exact gradient vanishes (a row with one visible key has P1 = P2 = 1),
+# a relative error is undefined; there the error is measured against an RMS
+# floor of 1e-4 per element instead.
+GRAD_FLOOR_RMS = 1e-4
+
+
 def assert_grad(got, ref, what=""):
-    e = rel_fro(got, ref)
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    denom = max(np.linalg.norm(ref), GRAD_FLOOR_RMS * np.sqrt(max(ref.size, 1)))
+    e = float(np.linalg.norm(got - ref) / denom)
     assert e <= GRAD_REL, f"{what}: relative Frobenius error {e:.3e}"
 
 
@@ -109,12 +118,19 @@ def oracle_rows(inp, w, rows, setting=None):
 
 
 def dk_invariants(dk, k_opt, dq, q_opt):
-    """sum_j dK_j = 0 per (b, h, d) and sum_i <dQ_i, Q_i> = sum_j <dK_j, K_j> per (b, h)."""
-    dk = dk.float()
+    """sum_j dK_j = 0 per (b, h, d) and sum_i <dQ_i, Q_i> = sum_j <dK_j, K_j> per (b, h).
+
+    Both sides are sums with heavy cancellation, so each residual is measured
+    against the magnitude of its terms (sum of |dK_j| per column, and the sum of
+    |<dQ_i, Q_i>| + |<dK_j, K_j>|), which is what bf16 output rounding scales with.
+    """
+    dk = dk.double()
     col = dk.sum(dim=2)  # [B, H, D]
     scale_ = dk.abs().sum(dim=2).clamp_min(1e-30)
     r_sum = float((col.abs() / scale_).max())
-    lhs = (dq.float() * q_opt.float()).sum(dim=(2, 3)).double()
-    rhs = (dk * k_opt.float()).sum(dim=(2, 3)).double()
-    r_tr = float(((lhs - rhs).abs() / torch.maximum(lhs.abs(), rhs.abs()).clamp_min(1e-30)).max())
+    tq = (dq.double() * q_opt.double()).sum(dim=3)  # [B, H, N_Q]
+    tk = (dk * k_opt.double()).sum(dim=3)  # [B, H, N_K]
+    lhs, rhs = tq.sum(dim=2), tk.sum(dim=2)
+    mag = (tq.abs().sum(dim=2) + tk.abs().sum(dim=2)).clamp_min(1e-30)
+    r_tr = float(((lhs - rhs).abs() / mag).max())
     return r_sum, r_tr

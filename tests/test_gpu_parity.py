@@ -112,12 +112,15 @@ def test_b2h32_n4096(name):
             for m, (dq, dk) in outs.items():
                 U.assert_grad(U.np64(dq[b, h]), rdq, f"setting {setting} mode {m} dQ head {b},{h}")
                 U.assert_grad(U.np64(dk[b, h]), rdk, f"setting {setting} mode {m} dK head {b},{h}")
+        # fused = separate on every head (separate is deterministic and checked above)
+        for which in (0, 1):
+            f, s_ = outs[skl.BWD_FUSED][which].double(), outs[skl.BWD_SEPARATE][which].double()
+            per_head = ((f - s_).norm(dim=(2, 3)) / s_.norm(dim=(2, 3)).clamp_min(1e-30)).max().item()
+            assert per_head < 1e-2, ("dQ" if which == 0 else "dK", per_head)
         qo, ko = (q2, k2) if setting == 1 else (q1, k1)
         for m, (dq, dk) in outs.items():
             r_sum, r_tr = U.dk_invariants(dk, ko, dq, qo)
-            assert r_sum < 2e-2 and r_tr < 2e-2, (m, r_sum, r_tr)
-        assert U.rel_fro(U.np64(outs[1][0]), U.np64(outs[2][0])) < 1e-2
-        assert U.rel_fro(U.np64(outs[1][1]), U.np64(outs[2][1])) < 1e-2
+            assert r_sum < 1e-2 and r_tr < 1e-2, (m, r_sum, r_tr)
 
 
 def test_b1h32_n65536_causal_setting1():
