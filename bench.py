@@ -26,10 +26,13 @@ if ROOT not in sys.path:
 
 import numpy as np  # noqa: E402
 
-# DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) of the
-# dominant kernel, from the ncu summary under profiles/ for the same kernel
-# build; None until measured or after the kernel changed.
-NCU_TRAFFIC_BYTES = {}
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of a launch,
+# divided by its algorithmic bytes, from the ncu summaries under profiles/ for
+# the current build of each kernel (scaled to a full launch by the units it
+# processes); absent until measured, and removed when the kernel changes.
+NCU_TRAFFIC_RATIO = {"splitk": 1.0012}  # profiles/splitk_partial_decode_b2h32_nq4_nk131072.md
+# For tensor-bound kernels: measured DRAM bytes per unmasked (query, key) pair.
+NCU_TRAFFIC_PER_PAIR = {}
 
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -56,7 +59,16 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--heads", type=int, default=0, help="override H (smaller cases for profiling)")
+    ap.add_argument("--batch", type=int, default=0, help="override B (smaller cases for profiling)")
     return ap.parse_args()
+
+
+def pick_workload(synth, args):
+    w = synth.WORKLOADS[args.workload]
+    if args.heads or args.batch:
+        w = w.with_(H=args.heads or w.H, B=args.batch or w.B, name=f"{w.name}[B={args.batch or w.B},H={args.heads or w.H}]")
+    return w
 
 
 def dist_env():
@@ -179,7 +191,7 @@ def run_reference(args):
         return 0
     from attention_kl_divergence_streamkl_gb300 import synth
     from oracle import oracle as O
-    w = synth.WORKLOADS[args.workload]
+    w = pick_workload(synth, args)
     decode = w.name.startswith("decode")
     q1, k1, q2, k2 = (synth.bf16_bits_to_f64(synth.head_slice(w, k, 0, 0)) for k in ("q1", "k1", "q2", "k2"))
     g = synth.upstream_grad(w)[0, 0].astype(np.float64)
@@ -234,7 +246,7 @@ def run_ours(args):
     import attention_kl_divergence_streamkl_gb300 as skl
     from attention_kl_divergence_streamkl_gb300 import synth
 
-    w = synth.WORKLOADS[args.workload]
+    w = pick_workload(synth, args)
     decode = w.name.startswith("decode")
     mode = {"auto": skl.BWD_AUTO, "fused": skl.BWD_FUSED, "separate": skl.BWD_SEPARATE}[args.bwd_mode]
     if not decode and mode == skl.BWD_AUTO:
@@ -334,7 +346,8 @@ def run_ours(args):
         dom = kernels[0]
         achieved = bytes_step / (per_kernel[dom] / args.steps / 1e3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved / peaks["hbm_gbs"], "traffic": NCU_TRAFFIC_BYTES.get(dom), "kernel": dom,
+                "frac": achieved / peaks["hbm_gbs"], "kernel": dom,
+                "traffic": NCU_TRAFFIC_RATIO[dom] * bytes_step if dom in NCU_TRAFFIC_RATIO else None,
                 "peak_source": f"{peak_src} hbm_gbs", "algorithmic_bytes_per_launch": bytes_step}
     else:
         flops_step = 12 * w.D * pairs
@@ -345,7 +358,7 @@ def run_ours(args):
         achieved = algo[dom] / (avg_ms / 1e3) / 1e12
         peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                "traffic": NCU_TRAFFIC_BYTES.get(dom), "kernel": dom,
+                "traffic": NCU_TRAFFIC_PER_PAIR[dom] * pairs if dom in NCU_TRAFFIC_PER_PAIR else None, "kernel": dom,
                 "peak_source": f"{peak_src} bf16_tflops_sustained (kernel timed inside a long step)",
                 "algorithmic_flops_per_launch": algo[dom],
                 "frac_of_burst_peak_whole_step": value / world / peaks["bf16_tflops"]}
