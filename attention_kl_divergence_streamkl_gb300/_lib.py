@@ -21,7 +21,7 @@ import torch
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libstreamkl.so")
 
-OK, ERR_INVALID, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT = range(6)
+OK, ERR_INVALID, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT, ERR_SCRATCH_LIMIT = range(7)
 BWD_AUTO, BWD_FUSED, BWD_SEPARATE, BWD_DQ_ONLY, BWD_DK_ONLY = 0, 1, 2, 3, 4
 SPLITK_MAX_NQ = 16
 
@@ -44,6 +44,7 @@ SIGNATURES = {
     "streamkl_fwd_splitk_workspace": (_I, [Shape, _I, ctypes.POINTER(_SZ)]),
     "streamkl_fwd_splitk": (_I, [_P, _P, _P, _P, Shape, _I, _P, _SZ, _F, _F, _F, _S]),
     "streamkl_fwd_splitk_plan": (_I, [Shape, _I, ctypes.POINTER(_I)]),
+    "streamkl_fwd_splitk_noalloc": (_I, [_P, _P, _P, _P, Shape, _I, _F, _F, _F, _S]),
     "streamkl_bwd_workspace": (_I, [Shape, _I, ctypes.POINTER(_SZ)]),
     "streamkl_bwd_select": (_I, [Shape, _SZ]),
     "streamkl_bwd_s1": (_I, [_P, _P, _P, _P, Shape, _F, _F, _F, _P, _P, _I, _P, _SZ, _S]),

@@ -142,6 +142,7 @@ const char* streamkl_status_string(streamkl_status st) {
     case STREAMKL_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
     case STREAMKL_ERR_CUDA: return "CUDA call failed";
     case STREAMKL_ERR_TIMEOUT: return "device-side wait timed out";
+    case STREAMKL_ERR_SCRATCH_LIMIT: return "problem needs more than the fixed no-allocation scratch";
   }
   return "unknown status";
 }
@@ -197,6 +198,27 @@ streamkl_status streamkl_fwd_splitk(const void* q1, const void* k1, const void* 
   if ((v = status_ptr(&status)) != STREAMKL_OK) return v;
   return from_cuda(launch_splitk(p, q1, k1, q2, k2, num_splits, static_cast<float*>(workspace), kl, lse1, lse2,
                                  status, static_cast<cudaStream_t>(stream)));
+}
+
+streamkl_status streamkl_fwd_splitk_noalloc(const void* q1, const void* k1, const void* q2, const void* k2,
+                                            streamkl_shape s, int num_splits, float* kl, float* lse1, float* lse2,
+                                            void* stream) {
+  Problem p;
+  streamkl_status v = validate(s, &p);
+  if (v != STREAMKL_OK) return v;
+  if (p.NQ > STREAMKL_SPLITK_MAX_NQ) return STREAMKL_ERR_UNSUPPORTED;
+  if (num_splits < 0 || num_splits > kMaxGridY) return STREAMKL_ERR_INVALID;
+  if (p.NQ == 0) return STREAMKL_OK;
+  if (!inputs_ok(q1, k1, q2, k2) || !rows_ok(kl) || !rows_ok(lse1) || !rows_ok(lse2)) return STREAMKL_ERR_INVALID;
+  if (num_splits == 0 && (v = streamkl_fwd_splitk_plan(s, 0, &num_splits)) != STREAMKL_OK) return v;
+  const size_t need = (size_t)p.BH * p.NQ * num_splits * 5 * sizeof(float);
+  if (need > STREAMKL_NOALLOC_SCRATCH_BYTES) return STREAMKL_ERR_SCRATCH_LIMIT;
+  float* scratch = nullptr;
+  if (splitk_noalloc_scratch(&scratch) != cudaSuccess) return STREAMKL_ERR_CUDA;
+  int* status = nullptr;
+  if ((v = status_ptr(&status)) != STREAMKL_OK) return v;
+  return from_cuda(launch_splitk(p, q1, k1, q2, k2, num_splits, scratch, kl, lse1, lse2, status,
+                                 static_cast<cudaStream_t>(stream)));
 }
 
 int streamkl_bwd_select(streamkl_shape s, size_t l2_bytes) {

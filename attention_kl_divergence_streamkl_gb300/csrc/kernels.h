@@ -33,6 +33,8 @@ int splitk_plan(int BH, int key_tiles, int num_sms);
 cudaError_t launch_splitk(const Problem& p, const void* q1, const void* k1, const void* q2, const void* k2,
                           int splits, float* partials, float* kl, float* lse1, float* lse2, int* status,
                           cudaStream_t st);
+// Device address (current device) of the fixed scratch of the allocation-free entry point.
+cudaError_t splitk_noalloc_scratch(float** out);
 
 // ---- backward ------------------------------------------------------------------
 struct BwdIn {

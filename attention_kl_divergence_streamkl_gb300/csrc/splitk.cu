@@ -16,8 +16,16 @@
 // queries on N, so a tile costs a handful of mma.sync per warp.  Each thread
 // keeps the running scalars of its queries and rescales only when a new
 // maximum exceeds the reference by more than 2^8 (exact: l1 and acc share m1).
+#include <atomic>
+
+#include "../../include/streamkl.h"
 #include "common.cuh"
 #include "kernels.h"
+
+// Fixed scratch of the allocation-free Split-K entry point: the partial states
+// of every split live here instead of in a caller-provided workspace.  Every
+// GPU that loads the library holds it until the process exits.
+static __device__ __align__(256) float g_splitk_noalloc_scratch[STREAMKL_NOALLOC_SCRATCH_BYTES / sizeof(float)];
 
 namespace skl {
 namespace {
@@ -335,6 +343,28 @@ cudaError_t launch_d(const Problem& p, const void* q1, const void* k1, const voi
 }  // namespace
 
 int splitk_key_tiles(const Problem& p) { return (p.NK + BN - 1) / BN; }
+
+// In host code the name g_splitk_noalloc_scratch is only a host-side stand-in;
+// the kernels need its device address, which the runtime gives per device.  It
+// is looked up once per device, with that device current, and kept.
+cudaError_t splitk_noalloc_scratch(float** out) {
+  constexpr int kMaxDevices = 64;
+  static std::atomic<float*> table[kMaxDevices];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  float* p = table[dev].load(std::memory_order_acquire);
+  if (!p) {
+    void* addr = nullptr;
+    e = cudaGetSymbolAddress(&addr, g_splitk_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    p = static_cast<float*>(addr);
+    table[dev].store(p, std::memory_order_release);
+  }
+  *out = p;
+  return cudaSuccess;
+}
 
 // Split count for BH heads of `key_tiles` tiles on `num_sms` SMs: minimises
 // waves x (tiles per block + a fixed per-block cost), where a wave is one

@@ -48,7 +48,8 @@ typedef enum {
   STREAMKL_ERR_UNSUPPORTED = 2, /* valid but not handled (e.g. D not in {64,128}, Split-K N_Q > 16) */
   STREAMKL_ERR_WORKSPACE = 3,   /* workspace pointer missing, misaligned or too small */
   STREAMKL_ERR_CUDA = 4,        /* a CUDA runtime/driver call failed (launch, memset, tensor map) */
-  STREAMKL_ERR_TIMEOUT = 5      /* a bounded device-side wait ran out (reported by check_device_status) */
+  STREAMKL_ERR_TIMEOUT = 5,     /* a bounded device-side wait ran out (reported by check_device_status) */
+  STREAMKL_ERR_SCRATCH_LIMIT = 6 /* needs more than the fixed scratch of streamkl_fwd_splitk_noalloc */
 } streamkl_status;
 
 /* Problem shape.  scale <= 0 means 1/sqrt(D). */
@@ -99,6 +100,31 @@ streamkl_status streamkl_fwd_splitk(const void* q1, const void* k1, const void* 
  * + a fixed per-block cost); with num_sms > 0 it is a pure host computation.
  */
 streamkl_status streamkl_fwd_splitk_plan(streamkl_shape s, int num_sms, int* num_splits);
+
+/*
+ * Split-K forward that allocates nothing and takes no workspace.  The paper
+ * has no counterpart of this entry point; it exists for callers that cannot
+ * call cudaMalloc or hand out scratch memory -- code that runs inside a host
+ * application or serving runtime owning all device memory, or a decode loop
+ * whose memory budget is fixed before it starts.  The caller still passes the
+ * inputs and outputs.
+ *
+ * The per-split partial states live in one static device array of
+ * STREAMKL_NOALLOC_SCRATCH_BYTES built into the library; every GPU that loads
+ * the library keeps it until the process exits.  A problem whose partials
+ * (B*H*N_Q*splits*5 floats) do not fit returns STREAMKL_ERR_SCRATCH_LIMIT with
+ * nothing launched.  All calls share that array and it keeps the last call's
+ * contents (each call overwrites every value it reads, so nothing needs
+ * clearing); calls that overlap on the GPU -- on different streams, or from
+ * different host threads -- race on it and must be serialised by the caller.
+ * The first call on a device looks up the array's device address with that
+ * device current (once per device); make that first call before any stream
+ * capture.  Results equal streamkl_fwd_splitk's for the same num_splits.
+ */
+#define STREAMKL_NOALLOC_SCRATCH_BYTES (4u << 20)
+streamkl_status streamkl_fwd_splitk_noalloc(const void* q1, const void* k1, const void* q2, const void* k2,
+                                            streamkl_shape s, int num_splits, float* kl, float* lse1,
+                                            float* lse2, void* stream);
 
 /*
  * Backward workspace: fused mode needs an fp32 [B,H,N_Q,D] dQ accumulator
