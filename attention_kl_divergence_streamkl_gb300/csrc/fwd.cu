@@ -1,86 +1,177 @@
-// One-pass attention-KL forward.
+// One-pass attention-KL forward on the 5th-generation tensor cores.
 //
 // StreamKL technical summary (gist.science/ja/paper/2606.20005), section 手法 1
-// "online formulation": each query row keeps five running scalars -- the two
-// running maxima m1, m2, the two unnormalised exponential sums l1, l2 and the
-// weighted logit-difference accumulator acc -- while key tiles stream through
-// on-chip memory; the row result is KL = acc/l1 + LSE2 - LSE1 with
-// LSE_t = m_t + log l_t, and key tiles wholly past the causal boundary are
-// never visited.
+// "online formulation": each query row keeps five running scalars (the running
+// maxima m1, m2, the unnormalised exponential sums l1, l2 and the weighted
+// logit-difference accumulator acc) while key tiles stream through on-chip
+// memory; the row result is KL = acc/l1 + LSE2 - LSE1 with LSE_t = m_t + log l_t,
+// and key tiles wholly past the causal boundary are never visited.
 //
-// Update rules used here (derived; the pages name the scalars but print no
-// update equations), per key tile, in log2 units x = c * (q . k), c = scale*log2 e:
-//     m1' = max(m1, max_j x1_j)          a1 = 2^(m1 - m1')
-//     l1  = a1 l1  + sum_j 2^(x1_j - m1')
-//     acc = a1 acc + sum_j 2^(x1_j - m1') (q1.k1_j - q2.k2_j)
-//     m2', l2 likewise from x2
-// and at the end LSE_t = ln2 (m_t + log2 l_t), KL = scale acc / l1 + LSE2 - LSE1.
+// Update rules (derived; the pages name the scalars but print no equations), in
+// log2 units x = c (q . k), c = scale log2(e), for the keys j of a tile:
+//     if max_j x1_j > m1 + 8:  a = 2^(m1 - max_j x1_j); l1 *= a; acc *= a; m1 = max_j x1_j
+//     l1  += sum_j 2^(x1_j - m1)
+//     acc += sum_j 2^(x1_j - m1) (q1.k1_j - q2.k2_j)
+//     m2, l2 likewise from x2
+// The maximum is only moved when it grows by more than 2^8 (terms stay <= 256,
+// far from fp32 overflow); this is exact because l1 and acc share m1.  At the
+// end LSE_t = ln2 (m_t + log2 l_t) and KL = scale acc / l1 + LSE2 - LSE1.
 //
-// Layout: one CTA per (b*h, 128-row query tile); 8 consumer warps own 16 rows
-// each, one producer warp feeds K1/K2 tiles of 64 keys through a 2-stage TMA
-// ring (128-byte swizzle).  The logits come from bf16 mma.sync into fp32
-// registers.  Query tiles are launched longest-first for causal balance.
+// Block layout (one 128-row query tile per block, key tiles of 128):
+//   warp 8      TMA producer: Q1, Q2 once, then K1/K2 tiles through 2 stages
+//   warp 9      TMEM owner (512 columns) and MMA issuer (one thread):
+//               S1 = Q1 K1^T and S2 = Q2 K2^T, M = N = 128, bf16 -> fp32 in
+//               TMEM, double-buffered (buffer b: S1 at 256b, S2 at 256b + 128)
+//   warps 0-7   two softmax warpgroups; thread = query row (TMEM lane), group
+//               g takes columns [64g, 64g + 64) of every tile and keeps its own
+//               five scalars; the groups merge in the epilogue.
+// Blocks are launched longest causal tile first, so the hardware's block
+// scheduler balances the triangle.
 #include "common.cuh"
 #include "kernels.h"
+#include "tc.cuh"
 
 namespace skl {
 namespace {
 
 constexpr int BM = 128;
-constexpr int BN = 64;
-constexpr int STAGES = 2;
-constexpr int CONSUMERS = 8;
-constexpr int THREADS = (CONSUMERS + 1) * 32;
+constexpr int BN = 128;
+constexpr int SOFTMAX_WARPS = 8;
+constexpr int PRODUCER_WARP = 8;
+constexpr int MMA_WARP = 9;
+constexpr int THREADS = 10 * 32;
+constexpr float kLazy = 8.0f;
+constexpr uint32_t kTmemCols = 512;
+constexpr int kOneBlockPerSmSmem = 120 * 1024;
 
 template <int D>
 struct Smem {
-  static constexpr int Q_BYTES = BM * D * 2;
+  static constexpr int Q_BYTES = BM * D * 2;  // one 128-row tile, D/64 halves of 16 KiB
   static constexpr int K_BYTES = BN * D * 2;
   static constexpr int OFF_Q1 = 0;
   static constexpr int OFF_Q2 = Q_BYTES;
-  static constexpr int OFF_K = 2 * Q_BYTES;
-  static constexpr int STAGE_BYTES = 2 * K_BYTES;
-  static constexpr int OFF_BAR = OFF_K + STAGES * STAGE_BYTES;
-  // bar_q, full[STAGES], empty[STAGES], abort flag
-  static constexpr int BYTES = OFF_BAR + 8 + 16 * STAGES + 16 + 1024;
+  static constexpr int OFF_K = 2 * Q_BYTES;  // stage s: K1 at OFF_K + s*STAGE, K2 after it
+  static constexpr int STAGE = 2 * K_BYTES;
+  static constexpr int OFF_MERGE = OFF_K + 2 * STAGE;  // [5][128] fp32 from group 1
+  static constexpr int OFF_BAR = OFF_MERGE + 5 * BM * 4;
+  // bar_q, full[2], empty[2], sfull[2], sfree[2], tmem slot, abort flag
+  static constexpr int BYTES = OFF_BAR + 8 * 9 + 16 + 1024;
 };
+
+struct Row5 {
+  float m1, m2, l1, l2, acc;
+};
+
+template <bool MASKED>
+__device__ __forceinline__ void online_update(Row5& st, uint32_t (&a0)[32], uint32_t (&a1)[32], uint32_t (&b0)[32],
+                                              uint32_t (&b1)[32], float c, int key0, int row_lim, int nk) {
+  // a*: raw S1 = q1.k1 (64 columns), b*: raw S2; key0 = key index of column 0
+  float mx1 = kNegInf, mx2 = kNegInf;
+  if (MASKED) {
+#pragma unroll
+    for (int i = 0; i < 64; ++i) {
+      const int key = key0 + i;
+      const bool keep = key < nk && key <= row_lim;
+      uint32_t& s1 = i < 32 ? a0[i] : a1[i - 32];
+      uint32_t& s2 = i < 32 ? b0[i] : b1[i - 32];
+      if (!keep) {
+        s1 = __float_as_uint(kNegInf);
+        s2 = __float_as_uint(kNegInf);
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    mx1 = fmaxf(mx1, fmaxf(__uint_as_float(a0[i]), __uint_as_float(a1[i])));
+    mx2 = fmaxf(mx2, fmaxf(__uint_as_float(b0[i]), __uint_as_float(b1[i])));
+  }
+  if (mx1 == kNegInf) return;  // every column of this tile is masked for this row
+  const float t1 = mx1 * c, t2 = mx2 * c;
+  if (t1 > st.m1 + kLazy) {
+    const float al = ex2(st.m1 - t1);
+    st.l1 *= al;
+    st.acc *= al;
+    st.m1 = t1;
+  }
+  if (t2 > st.m2 + kLazy) {
+    const float al = ex2(st.m2 - t2);
+    st.l2 *= al;
+    st.m2 = t2;
+  }
+  const float n1 = -st.m1, n2 = -st.m2;
+  float l1a = 0.f, l1b = 0.f, l2a = 0.f, l2b = 0.f, acca = 0.f, accb = 0.f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const float s1x = __uint_as_float(a0[i]), s1y = __uint_as_float(a1[i]);
+    const float s2x = __uint_as_float(b0[i]), s2y = __uint_as_float(b1[i]);
+    const float p1x = ex2(fmaf(s1x, c, n1)), p1y = ex2(fmaf(s1y, c, n1));
+    const float p2x = ex2(fmaf(s2x, c, n2)), p2y = ex2(fmaf(s2y, c, n2));
+    l1a += p1x;
+    l1b += p1y;
+    l2a += p2x;
+    l2b += p2y;
+    if (MASKED) {
+      // masked columns have p1 = 0 but s1 - s2 = -inf - -inf: keep them out
+      acca += p1x > 0.f ? p1x * (s1x - s2x) : 0.f;
+      accb += p1y > 0.f ? p1y * (s1y - s2y) : 0.f;
+    } else {
+      acca = fmaf(p1x, s1x - s2x, acca);
+      accb = fmaf(p1y, s1y - s2y, accb);
+    }
+  }
+  st.l1 += l1a + l1b;
+  st.l2 += l2a + l2b;
+  st.acc += acca + accb;
+}
 
 template <int D>
 __global__ void __launch_bounds__(THREADS, 1)
-    fwd_kernel(const Problem p, float* __restrict__ out_kl, float* __restrict__ out_lse1,
-               float* __restrict__ out_lse2, int* status, const __grid_constant__ CUtensorMap mq1,
-               const __grid_constant__ CUtensorMap mk1, const __grid_constant__ CUtensorMap mq2,
-               const __grid_constant__ CUtensorMap mk2) {
+    fwd_tc_kernel(const Problem p, float* __restrict__ out_kl, float* __restrict__ out_lse1,
+                  float* __restrict__ out_lse2, int* status, const __grid_constant__ CUtensorMap mq1,
+                  const __grid_constant__ CUtensorMap mk1, const __grid_constant__ CUtensorMap mq2,
+                  const __grid_constant__ CUtensorMap mk2) {
   using L = Smem<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   const uint32_t sb = smem_u32(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int bh = blockIdx.x;
-  const int qt = gridDim.y - 1 - blockIdx.y;  // longest causal tiles first
+  const int n_qt = (p.NQ + BM - 1) / BM;
+  const int bh = blockIdx.x % p.BH;
+  const int qt = n_qt - 1 - (int)(blockIdx.x / p.BH);  // longest causal tiles first
   const int q0 = qt * BM;
   const int q_last = min(p.NQ, q0 + BM) - 1;
   const int kend = p.causal ? min(p.NK, q_last + p.off + 1) : p.NK;
   const int n_kt = (kend + BN - 1) / BN;
 
   const uint32_t bar_q = sb + L::OFF_BAR;
-  const uint32_t bar_full = bar_q + 8;
-  const uint32_t bar_empty = bar_full + 8 * STAGES;
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_BAR + 8 + 16 * STAGES);
+  const uint32_t bar_full = bar_q + 8;     // [2]
+  const uint32_t bar_empty = bar_q + 24;   // [2]
+  const uint32_t bar_sfull = bar_q + 40;   // [2]
+  const uint32_t bar_sfree = bar_q + 56;   // [2]
+  const uint32_t tmem_slot = bar_q + 72;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_BAR + 76);
 
   if (threadIdx.x == 0) {
     mbar_init(bar_q, 1);
-    for (int s = 0; s < STAGES; ++s) {
+    for (int s = 0; s < 2; ++s) {
       mbar_init(bar_full + 8 * s, 1);
-      mbar_init(bar_empty + 8 * s, CONSUMERS);
+      mbar_init(bar_empty + 8 * s, 1);
+      mbar_init(bar_sfull + 8 * s, 1);
+      mbar_init(bar_sfree + 8 * s, SOFTMAX_WARPS);
     }
     *abort_flag = 0;
     fence_mbar_init();
   }
+  if (warp == MMA_WARP) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
   __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::OFF_BAR + 72);
 
-  if (warp == CONSUMERS) {
-    // ------------------------------------------------------------ producer
+  if (warp == PRODUCER_WARP) {
     if (lane == 0) {
       prefetch_tensormap(&mq1);
       prefetch_tensormap(&mk1);
@@ -93,162 +184,139 @@ __global__ void __launch_bounds__(THREADS, 1)
         tma_load_3d(sb + L::OFF_Q2 + h * BM * 128, &mq2, bar_q, h * 64, q0, bh);
       }
       int issued = 0;
-      for (int it = 0; it < n_kt; ++it) {
-        const int s = it % STAGES;
-        if (it >= STAGES && !mbar_wait(bar_empty + 8 * s, ((it / STAGES) - 1) & 1, status, abort_flag)) break;
-        const uint32_t kb = sb + L::OFF_K + s * L::STAGE_BYTES;
-        mbar_arrive_expect_tx(bar_full + 8 * s, L::STAGE_BYTES);
+      for (int j = 0; j < n_kt; ++j) {
+        const int s = j & 1;
+        if (j >= 2 && !mbar_wait(bar_empty + 8 * s, ((j >> 1) - 1) & 1, status, abort_flag)) break;
+        const uint32_t kb = sb + L::OFF_K + s * L::STAGE;
+        mbar_arrive_expect_tx(bar_full + 8 * s, L::STAGE);
 #pragma unroll
         for (int h = 0; h < D / 64; ++h) {
-          tma_load_3d(kb + h * BN * 128, &mk1, bar_full + 8 * s, h * 64, it * BN, bh);
-          tma_load_3d(kb + L::K_BYTES + h * BN * 128, &mk2, bar_full + 8 * s, h * 64, it * BN, bh);
+          tma_load_3d(kb + h * BN * 128, &mk1, bar_full + 8 * s, h * 64, j * BN, bh);
+          tma_load_3d(kb + L::K_BYTES + h * BN * 128, &mk2, bar_full + 8 * s, h * 64, j * BN, bh);
         }
-        issued = it + 1;
+        issued = j + 1;
       }
-      // Do not leave while copies may still land in this block's shared memory.
       mbar_drain(bar_q, 0, status);
-      for (int it = max(0, issued - STAGES); it < issued; ++it)
-        mbar_drain(bar_full + 8 * (it % STAGES), (it / STAGES) & 1, status);
-    }
-    return;
-  }
-
-  // -------------------------------------------------------------- consumers
-  const int g = lane >> 2, t = lane & 3;
-  const int row0 = q0 + warp * 16 + g;  // this thread's rows: row0, row0 + 8
-  const float c = p.c;
-  float m1[2] = {kNegInf, kNegInf}, m2[2] = {kNegInf, kNegInf};
-  float l1[2] = {0.f, 0.f}, l2[2] = {0.f, 0.f}, acc[2] = {0.f, 0.f};
-  bool ok = mbar_wait(bar_q, 0, status, abort_flag);
-
-  const int arow = warp * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-  const int acol = lane >> 4;
-  const int brow = (lane & 7) + (lane >> 4) * 8;
-  const int bcol = (lane >> 3) & 1;
-
-  for (int it = 0; ok && it < n_kt; ++it) {
-    const int s = it % STAGES;
-    if (!mbar_wait(bar_full + 8 * s, (it / STAGES) & 1, status, abort_flag)) {
-      ok = false;
-      break;
-    }
-    const uint32_t kb1 = sb + L::OFF_K + s * L::STAGE_BYTES;
-    const uint32_t kb2 = kb1 + L::K_BYTES;
-    float s1[8][4], s2[8][4];
-#pragma unroll
-    for (int n = 0; n < 8; ++n)
-#pragma unroll
-      for (int j = 0; j < 4; ++j) s1[n][j] = s2[n][j] = 0.f;
-
-#pragma unroll
-    for (int ks = 0; ks < D / 16; ++ks) {
-      uint32_t a1[4], a2[4];
-      ldsm_x4(sw128<BM>(sb + L::OFF_Q1, arow, 2 * ks + acol), a1);
-      ldsm_x4(sw128<BM>(sb + L::OFF_Q2, arow, 2 * ks + acol), a2);
-#pragma unroll
-      for (int np = 0; np < 4; ++np) {
-        uint32_t b[4];
-        ldsm_x4(sw128<BN>(kb1, np * 16 + brow, 2 * ks + bcol), b);
-        mma16816(s1[2 * np], a1, b[0], b[1]);
-        mma16816(s1[2 * np + 1], a1, b[2], b[3]);
-        ldsm_x4(sw128<BN>(kb2, np * 16 + brow, 2 * ks + bcol), b);
-        mma16816(s2[2 * np], a2, b[0], b[1]);
-        mma16816(s2[2 * np + 1], a2, b[2], b[3]);
-      }
+      for (int j = max(0, issued - 2); j < issued; ++j) mbar_drain(bar_full + 8 * (j & 1), (j >> 1) & 1, status);
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(bar_empty + 8 * s);
-
-    // ---- online update of the five scalars for rows row0 and row0 + 8
-    const int kbase = it * BN;
-    const bool need_mask = (kbase + BN > p.NK) || (p.causal && kbase + BN - 1 > q0 + p.off);
+  } else if (warp == MMA_WARP) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16(BM, BN, false, false);
+      int issued = 0;
+      bool ok = mbar_wait(bar_q, 0, status, abort_flag);
+      for (int j = 0; ok && j < n_kt; ++j) {
+        const int s = j & 1;
+        if (!mbar_wait(bar_full + 8 * s, (j >> 1) & 1, status, abort_flag)) break;
+        if (j >= 2 && !mbar_wait(bar_sfree + 8 * s, ((j >> 1) - 1) & 1, status, abort_flag)) break;
+        tc_fence_after();
+        const uint32_t kb1 = sb + L::OFF_K + s * L::STAGE, kb2 = kb1 + L::K_BYTES;
+        const uint32_t d1 = tmem + s * 256, d2 = d1 + 128;
 #pragma unroll
-    for (int hr = 0; hr < 2; ++hr) {
-      const int row = row0 + hr * 8;
-      float v1[16], v2[16], d[16];
-      float mx1 = kNegInf, mx2 = kNegInf;
-#pragma unroll
-      for (int n = 0; n < 8; ++n)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int i = n * 2 + e;
-          v1[i] = s1[n][2 * hr + e];
-          v2[i] = s2[n][2 * hr + e];
-          d[i] = v1[i] - v2[i];
-          if (need_mask) {
-            const int key = kbase + n * 8 + 2 * t + e;
-            const bool keep = key < p.NK && (!p.causal || key <= row + p.off);
-            if (!keep) {
-              v1[i] = kNegInf;
-              v2[i] = kNegInf;
-              d[i] = 0.f;
-            }
-          }
-          mx1 = fmaxf(mx1, v1[i]);
-          mx2 = fmaxf(mx2, v2[i]);
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t off = (ks >> 2) * (BM * 128) + (ks & 3) * 32;  // BM == BN: same half stride
+          mma_ss(d1, sdesc_sw128(sb + L::OFF_Q1 + off, 0, 1024), sdesc_sw128(kb1 + off, 0, 1024), idesc, ks > 0);
         }
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-      mx2 = fmaxf(mx2, __shfl_xor_sync(0xffffffffu, mx2, 1));
-      mx2 = fmaxf(mx2, __shfl_xor_sync(0xffffffffu, mx2, 2));
-      const float n1 = fmaxf(m1[hr], mx1 * c);
-      const float n2 = fmaxf(m2[hr], mx2 * c);
-      const float b1 = n1 == kNegInf ? 0.f : n1;  // all keys masked so far: weights stay 0
-      const float b2 = n2 == kNegInf ? 0.f : n2;
-      const float a1 = ex2(m1[hr] - b1);
-      const float a2 = ex2(m2[hr] - b2);
-      float sl1 = 0.f, sl2 = 0.f, sacc = 0.f;
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const float p1 = ex2(fmaf(v1[i], c, -b1));
-        const float p2 = ex2(fmaf(v2[i], c, -b2));
-        sl1 += p1;
-        sl2 += p2;
-        sacc = fmaf(p1, d[i], sacc);
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t off = (ks >> 2) * (BM * 128) + (ks & 3) * 32;
+          mma_ss(d2, sdesc_sw128(sb + L::OFF_Q2 + off, 0, 1024), sdesc_sw128(kb2 + off, 0, 1024), idesc, ks > 0);
+        }
+        mma_commit(bar_sfull + 8 * s);
+        mma_commit(bar_empty + 8 * s);
+        issued = j + 1;
       }
-      l1[hr] = fmaf(l1[hr], a1, sl1);
-      acc[hr] = fmaf(acc[hr], a1, sacc);
-      l2[hr] = fmaf(l2[hr], a2, sl2);
-      m1[hr] = n1;
-      m2[hr] = n2;
+      // the last commit completes once every MMA issued here has finished
+      if (issued > 0) mbar_drain(bar_sfull + 8 * ((issued - 1) & 1), ((issued - 1) >> 1) & 1, status);
     }
-  }
-  if (!ok) return;
-
-  // ---- epilogue: the quad shares the running maxima, so sums simply add
-#pragma unroll
-  for (int hr = 0; hr < 2; ++hr) {
-    float L1 = l1[hr], L2 = l2[hr], A = acc[hr];
-    L1 += __shfl_xor_sync(0xffffffffu, L1, 1);
-    L1 += __shfl_xor_sync(0xffffffffu, L1, 2);
-    L2 += __shfl_xor_sync(0xffffffffu, L2, 1);
-    L2 += __shfl_xor_sync(0xffffffffu, L2, 2);
-    A += __shfl_xor_sync(0xffffffffu, A, 1);
-    A += __shfl_xor_sync(0xffffffffu, A, 2);
-    const int row = row0 + hr * 8;
-    if (t == 0 && row < p.NQ) {
-      const float lse1 = (m1[hr] + log2f(L1)) * kLn2;
-      const float lse2 = (m2[hr] + log2f(L2)) * kLn2;
+    __syncwarp();
+  } else {
+    // ---------------------------------------------------------- softmax groups
+    const int grp = warp >> 2, wq = warp & 3;
+    const int r = wq * 32 + lane;  // row within the tile = TMEM lane
+    const int row = q0 + r;
+    const int row_lim = row + p.off;  // last key this row keeps when causal
+    const float c = p.c;
+    Row5 st{kNegInf, kNegInf, 0.f, 0.f, 0.f};
+    bool ok = true;
+    for (int j = 0; j < n_kt; ++j) {
+      const int s = j & 1;
+      const bool got = mbar_wait(bar_sfull + 8 * s, (j >> 1) & 1, status, abort_flag);
+      __syncwarp();
+      if (!got) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t ta = tmem + ((uint32_t)(wq * 32) << 16) + s * 256 + grp * 64;
+      uint32_t a0[32], a1[32], b0[32], b1[32];
+      tmem_ld32(ta, a0);
+      tmem_ld32(ta + 32, a1);
+      tmem_ld32(ta + 128, b0);
+      tmem_ld32(ta + 160, b1);
+      tmem_ld_wait();
+      reg_fence32(a0);
+      reg_fence32(a1);
+      reg_fence32(b0);
+      reg_fence32(b1);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_sfree + 8 * s);
+      const int key0 = j * BN + grp * 64;
+      const bool masked = (key0 + 63 >= p.NK) || (p.causal && key0 + 63 > row_lim);
+      if (masked)
+        online_update<true>(st, a0, a1, b0, b1, c, key0, p.causal ? row_lim : 0x7fffffff, p.NK);
+      else
+        online_update<false>(st, a0, a1, b0, b1, c, key0, 0, p.NK);
+    }
+    // ---- merge the two column groups, then the closing step of the forward
+    float* mrg = reinterpret_cast<float*>(smem + L::OFF_MERGE);
+    if (grp == 1) {
+      mrg[0 * BM + r] = st.m1;
+      mrg[1 * BM + r] = st.m2;
+      mrg[2 * BM + r] = st.l1;
+      mrg[3 * BM + r] = st.l2;
+      mrg[4 * BM + r] = st.acc;
+    }
+    named_bar_sync(1, SOFTMAX_WARPS * 32);
+    if (grp == 0 && ok && !*abort_flag && row < p.NQ) {
+      const float om1 = mrg[r], om2 = mrg[BM + r], ol1 = mrg[2 * BM + r], ol2 = mrg[3 * BM + r],
+                  oacc = mrg[4 * BM + r];
+      const float M1 = fmaxf(st.m1, om1), M2 = fmaxf(st.m2, om2);
+      const float wa1 = ex2(st.m1 - M1), wb1 = ex2(om1 - M1);
+      const float wa2 = ex2(st.m2 - M2), wb2 = ex2(om2 - M2);
+      const float l1 = st.l1 * wa1 + ol1 * wb1, acc = st.acc * wa1 + oacc * wb1;
+      const float l2 = st.l2 * wa2 + ol2 * wb2;
+      const float lse1 = (M1 + log2f(l1)) * kLn2;
+      const float lse2 = (M2 + log2f(l2)) * kLn2;
       const size_t o = (size_t)bh * p.NQ + row;
       out_lse1[o] = lse1;
       out_lse2[o] = lse2;
-      out_kl[o] = p.scale * (A / L1) + lse2 - lse1;
+      out_kl[o] = p.scale * (acc / l1) + lse2 - lse1;
     }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == MMA_WARP) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
   }
 }
 
 template <int D>
-cudaError_t launch_fwd_d(const Problem& p, const void* q1, const void* k1, const void* q2, const void* k2,
-                         float* kl, float* lse1, float* lse2, int* status, cudaStream_t st) {
+cudaError_t launch_d(const Problem& p, const void* q1, const void* k1, const void* q2, const void* k2, float* kl,
+                     float* lse1, float* lse2, int* status, cudaStream_t st) {
   CUtensorMap mq1, mk1, mq2, mk2;
   if (!encode_tile_map(&mq1, q1, D, p.NQ, p.BH, BM) || !encode_tile_map(&mq2, q2, D, p.NQ, p.BH, BM) ||
       !encode_tile_map(&mk1, k1, D, p.NK, p.BH, BN) || !encode_tile_map(&mk2, k2, D, p.NK, p.BH, BN))
     return cudaErrorInvalidValue;
-  const int smem = Smem<D>::BYTES;
-  cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  // A block owns all 512 TMEM columns: ask for enough shared memory that a
+  // second block never shares the SM (it would only wait in tcgen05.alloc).
+  const int smem = Smem<D>::BYTES > kOneBlockPerSmSmem ? Smem<D>::BYTES : kOneBlockPerSmSmem;
+  cudaError_t e = cudaFuncSetAttribute(fwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  dim3 grid(p.BH, (p.NQ + BM - 1) / BM);
-  fwd_kernel<D><<<grid, THREADS, smem, st>>>(p, kl, lse1, lse2, status, mq1, mk1, mq2, mk2);
+  const long long blocks = (long long)p.BH * ((p.NQ + BM - 1) / BM);
+  fwd_tc_kernel<D><<<(unsigned)blocks, THREADS, smem, st>>>(p, kl, lse1, lse2, status, mq1, mk1, mq2, mk2);
   return cudaGetLastError();
 }
 
@@ -256,8 +324,8 @@ cudaError_t launch_fwd_d(const Problem& p, const void* q1, const void* k1, const
 
 cudaError_t launch_fwd(const Problem& p, const void* q1, const void* k1, const void* q2, const void* k2,
                        float* kl, float* lse1, float* lse2, int* status, cudaStream_t st) {
-  if (p.D == 64) return launch_fwd_d<64>(p, q1, k1, q2, k2, kl, lse1, lse2, status, st);
-  return launch_fwd_d<128>(p, q1, k1, q2, k2, kl, lse1, lse2, status, st);
+  if (p.D == 64) return launch_d<64>(p, q1, k1, q2, k2, kl, lse1, lse2, status, st);
+  return launch_d<128>(p, q1, k1, q2, k2, kl, lse1, lse2, status, st);
 }
 
 }  // namespace skl
