@@ -12,11 +12,12 @@
 //     setting 2:  dS1 = g_i P1 (r - KL_i),  r = (S1 - LSE1) - (S2 - LSE2)
 // and for the optimised pair dQ = scale dS K, dK = scale dS^T Q.
 //
-// Two paths (section 手法 2 "kernel fusion"): the fused one visits each
-// (query tile, key tile) pair once from a key-stationary block and adds the
-// dQ contribution into an fp32 buffer with vector atomics (used while that
-// buffer fits in L2); the separate one runs a query-stationary dQ kernel and a
-// key-stationary dK kernel, each rebuilding the probabilities.
+// This file holds the fused path (section 手法 2 "kernel fusion"): each
+// (query tile, key tile) pair is visited once from a key-stationary block, dK
+// accumulates in registers and the dQ contribution is added into an fp32
+// buffer with vector atomics, which the library uses while that buffer fits in
+// L2.  The separate path (a query-stationary dQ kernel and a key-stationary dK
+// kernel on tcgen05) is in bwd_tc.cu.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -26,195 +27,6 @@ namespace {
 constexpr int CONSUMERS = 8;
 constexpr int THREADS = (CONSUMERS + 1) * 32;
 constexpr int STAGES = 2;
-
-// ============================================================================
-// dQ kernel: one block per (b*h, 128-row query tile), streams 64-key tiles
-// ============================================================================
-constexpr int QBM = 128;
-constexpr int QBN = 64;
-
-template <int D>
-struct DqSmem {
-  static constexpr int Q_BYTES = QBM * D * 2;
-  static constexpr int K_BYTES = QBN * D * 2;
-  static constexpr int OFF_Q1 = 0;
-  static constexpr int OFF_Q2 = Q_BYTES;
-  static constexpr int OFF_K = 2 * Q_BYTES;
-  static constexpr int STAGE_BYTES = 2 * K_BYTES;
-  static constexpr int OFF_BAR = OFF_K + STAGES * STAGE_BYTES;
-  static constexpr int BYTES = OFF_BAR + 8 + 16 * STAGES + 16 + 1024;
-};
-
-template <int D, int SETTING>
-__global__ void __launch_bounds__(THREADS, 1)
-    bwd_dq_kernel(const Problem p, const float* __restrict__ lse1, const float* __restrict__ lse2,
-                  const float* __restrict__ klv, const float* __restrict__ gv, __nv_bfloat16* __restrict__ dq_out,
-                  int* status, const __grid_constant__ CUtensorMap mq1, const __grid_constant__ CUtensorMap mk1,
-                  const __grid_constant__ CUtensorMap mq2, const __grid_constant__ CUtensorMap mk2) {
-  using L = DqSmem<D>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = align1024(smem_raw);
-  const uint32_t sb = smem_u32(smem);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int bh = blockIdx.x;
-  const int qt = gridDim.y - 1 - blockIdx.y;
-  const int q0 = qt * QBM;
-  const int q_last = min(p.NQ, q0 + QBM) - 1;
-  const int kend = p.causal ? min(p.NK, q_last + p.off + 1) : p.NK;
-  const int n_kt = (kend + QBN - 1) / QBN;
-
-  const uint32_t bar_q = sb + L::OFF_BAR;
-  const uint32_t bar_full = bar_q + 8;
-  const uint32_t bar_empty = bar_full + 8 * STAGES;
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_BAR + 8 + 16 * STAGES);
-  if (threadIdx.x == 0) {
-    mbar_init(bar_q, 1);
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(bar_full + 8 * s, 1);
-      mbar_init(bar_empty + 8 * s, CONSUMERS);
-    }
-    *abort_flag = 0;
-    fence_mbar_init();
-  }
-  __syncthreads();
-
-  if (warp == CONSUMERS) {
-    if (lane == 0) {
-      mbar_arrive_expect_tx(bar_q, 2 * L::Q_BYTES);
-#pragma unroll
-      for (int h = 0; h < D / 64; ++h) {
-        tma_load_3d(sb + L::OFF_Q1 + h * QBM * 128, &mq1, bar_q, h * 64, q0, bh);
-        tma_load_3d(sb + L::OFF_Q2 + h * QBM * 128, &mq2, bar_q, h * 64, q0, bh);
-      }
-      int issued = 0;
-      for (int it = 0; it < n_kt; ++it) {
-        const int s = it % STAGES;
-        if (it >= STAGES && !mbar_wait(bar_empty + 8 * s, ((it / STAGES) - 1) & 1, status, abort_flag)) break;
-        const uint32_t kb = sb + L::OFF_K + s * L::STAGE_BYTES;
-        mbar_arrive_expect_tx(bar_full + 8 * s, L::STAGE_BYTES);
-#pragma unroll
-        for (int h = 0; h < D / 64; ++h) {
-          tma_load_3d(kb + h * QBN * 128, &mk1, bar_full + 8 * s, h * 64, it * QBN, bh);
-          tma_load_3d(kb + L::K_BYTES + h * QBN * 128, &mk2, bar_full + 8 * s, h * 64, it * QBN, bh);
-        }
-        issued = it + 1;
-      }
-      mbar_drain(bar_q, 0, status);
-      for (int it = max(0, issued - STAGES); it < issued; ++it)
-        mbar_drain(bar_full + 8 * (it % STAGES), (it / STAGES) & 1, status);
-    }
-    return;
-  }
-
-  const int g = lane >> 2, t = lane & 3;
-  const int row0 = q0 + warp * 16 + g;
-  const float c = p.c;
-  float Lse1[2], Lse2[2], G[2], KLr[2];
-#pragma unroll
-  for (int hr = 0; hr < 2; ++hr) {
-    const int row = row0 + hr * 8;
-    const bool in = row < p.NQ;
-    const size_t o = (size_t)bh * p.NQ + row;
-    Lse1[hr] = in ? lse1[o] * kLog2e : 0.f;
-    Lse2[hr] = in ? lse2[o] * kLog2e : 0.f;
-    G[hr] = in ? gv[o] : 0.f;
-    KLr[hr] = (SETTING == 2 && in) ? klv[o] : 0.f;
-  }
-  float dq[D / 8][4];
-#pragma unroll
-  for (int n = 0; n < D / 8; ++n)
-#pragma unroll
-    for (int j = 0; j < 4; ++j) dq[n][j] = 0.f;
-
-  bool ok = mbar_wait(bar_q, 0, status, abort_flag);
-  const int arow = warp * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-  const int acol = lane >> 4;
-  const int brow = (lane & 7) + (lane >> 4) * 8;
-  const int bcol = (lane >> 3) & 1;
-  const int trow = (lane & 7) + ((lane >> 3) & 1) * 8;  // ldmatrix.trans rows
-  const int tcol = lane >> 4;
-
-  for (int it = 0; ok && it < n_kt; ++it) {
-    const int s = it % STAGES;
-    if (!mbar_wait(bar_full + 8 * s, (it / STAGES) & 1, status, abort_flag)) {
-      ok = false;
-      break;
-    }
-    const uint32_t kb1 = sb + L::OFF_K + s * L::STAGE_BYTES;
-    const uint32_t kb2 = kb1 + L::K_BYTES;
-    float s1[8][4], s2[8][4];
-#pragma unroll
-    for (int n = 0; n < 8; ++n)
-#pragma unroll
-      for (int j = 0; j < 4; ++j) s1[n][j] = s2[n][j] = 0.f;
-#pragma unroll
-    for (int ks = 0; ks < D / 16; ++ks) {
-      uint32_t a1[4], a2[4];
-      ldsm_x4(sw128<QBM>(sb + L::OFF_Q1, arow, 2 * ks + acol), a1);
-      ldsm_x4(sw128<QBM>(sb + L::OFF_Q2, arow, 2 * ks + acol), a2);
-#pragma unroll
-      for (int np = 0; np < 4; ++np) {
-        uint32_t b[4];
-        ldsm_x4(sw128<QBN>(kb1, np * 16 + brow, 2 * ks + bcol), b);
-        mma16816(s1[2 * np], a1, b[0], b[1]);
-        mma16816(s1[2 * np + 1], a1, b[2], b[3]);
-        ldsm_x4(sw128<QBN>(kb2, np * 16 + brow, 2 * ks + bcol), b);
-        mma16816(s2[2 * np], a2, b[0], b[1]);
-        mma16816(s2[2 * np + 1], a2, b[2], b[3]);
-      }
-    }
-    // dS for this tile, packed straight into bf16 A fragments (k = keys)
-    const int kbase = it * QBN;
-    const bool need_mask = (kbase + QBN > p.NK) || (p.causal && kbase + QBN - 1 > q0 + p.off);
-    uint32_t af[4][4];
-#pragma unroll
-    for (int n = 0; n < 8; ++n) {
-      float ds[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int hr = j >> 1;
-        const int key = kbase + n * 8 + 2 * t + (j & 1);
-        const bool keep = !need_mask || (key < p.NK && (!p.causal || key <= row0 + hr * 8 + p.off));
-        const float p1 = keep ? ex2(fmaf(s1[n][j], c, -Lse1[hr])) : 0.f;
-        if (SETTING == 1) {
-          const float p2 = keep ? ex2(fmaf(s2[n][j], c, -Lse2[hr])) : 0.f;
-          ds[j] = G[hr] * (p2 - p1);
-        } else {
-          const float r = kLn2 * fmaf(s1[n][j] - s2[n][j], c, Lse2[hr] - Lse1[hr]);
-          ds[j] = G[hr] * p1 * (r - KLr[hr]);
-        }
-      }
-      af[n >> 1][2 * (n & 1) + 0] = pack_bf16(ds[0], ds[1]);
-      af[n >> 1][2 * (n & 1) + 1] = pack_bf16(ds[2], ds[3]);
-    }
-    // dQ += dS K_opt
-    const uint32_t kopt = SETTING == 1 ? kb2 : kb1;
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-#pragma unroll
-      for (int np = 0; np < D / 16; ++np) {
-        uint32_t b[4];
-        ldsm_x4_t(sw128<QBN>(kopt, kk * 16 + trow, 2 * np + tcol), b);
-        mma16816(dq[2 * np], af[kk], b[0], b[1]);
-        mma16816(dq[2 * np + 1], af[kk], b[2], b[3]);
-      }
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(bar_empty + 8 * s);
-  }
-  if (!ok) return;
-#pragma unroll
-  for (int hr = 0; hr < 2; ++hr) {
-    const int row = row0 + hr * 8;
-    if (row < p.NQ) {
-      __nv_bfloat16* dst = dq_out + ((size_t)bh * p.NQ + row) * D + 2 * t;
-#pragma unroll
-      for (int n = 0; n < D / 8; ++n)
-        *reinterpret_cast<uint32_t*>(dst + n * 8) =
-            pack_bf16(dq[n][2 * hr] * p.scale, dq[n][2 * hr + 1] * p.scale);
-    }
-  }
-}
 
 // ============================================================================
 // dK kernel (and fused dK + dQ-atomics): one block per (b*h, 128-key tile),
@@ -483,21 +295,8 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const float4* __restric
   }
 }
 
-template <int D, int SETTING>
-cudaError_t launch_dq(const Problem& p, const BwdIn& in, void* dq, int* status, cudaStream_t st) {
-  CUtensorMap mq1, mk1, mq2, mk2;
-  if (!encode_tile_map(&mq1, in.q1, D, p.NQ, p.BH, QBM) || !encode_tile_map(&mq2, in.q2, D, p.NQ, p.BH, QBM) ||
-      !encode_tile_map(&mk1, in.k1, D, p.NK, p.BH, QBN) || !encode_tile_map(&mk2, in.k2, D, p.NK, p.BH, QBN))
-    return cudaErrorInvalidValue;
-  const int smem = DqSmem<D>::BYTES;
-  auto kern = bwd_dq_kernel<D, SETTING>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
-  kern<<<dim3(p.BH, (p.NQ + QBM - 1) / QBM), THREADS, smem, st>>>(
-      p, in.lse1, in.lse2, in.kl, in.g, static_cast<__nv_bfloat16*>(dq), status, mq1, mk1, mq2, mk2);
-  return cudaGetLastError();
-}
-
+// FUSED = false is the separate-path dK form of the same loop; only the fused
+// form is launched (the separate path runs on tcgen05, bwd_tc.cu).
 template <int D, int SETTING, bool FUSED>
 cudaError_t launch_dk(const Problem& p, const BwdIn& in, void* dk, float* dq_acc, int* status, cudaStream_t st) {
   CUtensorMap mq1, mk1, mq2, mk2;
@@ -511,18 +310,6 @@ cudaError_t launch_dk(const Problem& p, const BwdIn& in, void* dk, float* dq_acc
   kern<<<dim3(p.BH, (p.NK + KBK - 1) / KBK), THREADS, smem, st>>>(
       p, in.lse1, in.lse2, in.kl, in.g, static_cast<__nv_bfloat16*>(dk), dq_acc, status, mq1, mk1, mq2, mk2);
   return cudaGetLastError();
-}
-
-template <int D>
-cudaError_t separate_d(const Problem& p, int setting, const BwdIn& in, void* dq, void* dk, int* status,
-                       cudaStream_t st) {
-  if (dq) {
-    cudaError_t e = setting == 1 ? launch_dq<D, 1>(p, in, dq, status, st) : launch_dq<D, 2>(p, in, dq, status, st);
-    if (e != cudaSuccess) return e;
-  }
-  if (!dk) return cudaSuccess;
-  return setting == 1 ? launch_dk<D, 1, false>(p, in, dk, nullptr, status, st)
-                      : launch_dk<D, 2, false>(p, in, dk, nullptr, status, st);
 }
 
 template <int D>
@@ -542,12 +329,6 @@ cudaError_t fused_d(const Problem& p, int setting, const BwdIn& in, void* dq, vo
 }
 
 }  // namespace
-
-cudaError_t launch_bwd_separate(const Problem& p, int setting, const BwdIn& in, void* dq, void* dk, int* status,
-                                cudaStream_t st) {
-  if (p.D == 64) return separate_d<64>(p, setting, in, dq, dk, status, st);
-  return separate_d<128>(p, setting, in, dq, dk, status, st);
-}
 
 cudaError_t launch_bwd_fused(const Problem& p, int setting, const BwdIn& in, void* dq, void* dk, float* dq_acc,
                              int* status, cudaStream_t st) {

@@ -75,6 +75,22 @@ def dist_env():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
 
 
+def max_over_ranks(value: float, device) -> float:
+    """The largest `value` over all ranks (the job's time is its slowest rank's)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(work_per_rank: float, ms_per_step: float, world: int, unit_scale: float) -> float:
+    """Aggregate rate: every rank does `work_per_rank` per step in (max-over-ranks) `ms_per_step`."""
+    return world * work_per_rank / (ms_per_step / 1e3) / unit_scale
+
+
 # ----------------------------------------------------------------------------- clocks
 
 class ClockSampler:
@@ -332,16 +348,13 @@ def run_ours(args):
     status = skl.check_device_status(dev)
     assert status == 0, f"device-side timeout in the timed region (status {status})"
 
-    if world > 1:
-        t = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(elapsed_ms, dev)
 
     peaks, peak_src = load_peaks()
     ms_step = elapsed_ms / args.steps
     if decode:
         bytes_step = 2 * w.B * w.H * w.NK * w.D * 2 + 2 * w.B * w.H * w.NQ * w.D * 2
-        value = world * bytes_step / (ms_step / 1e3) / 1e9
+        value = whole_job_rate(bytes_step, ms_step, world, 1e9)
         metric, unit = "attn-KL split-K decode fwd GB/s (B8 H32 N_K=131072 D128)", "GB/s"
         dom = kernels[0]
         achieved = bytes_step / (per_kernel[dom] / args.steps / 1e3) / 1e9
@@ -351,7 +364,7 @@ def run_ours(args):
                 "peak_source": f"{peak_src} hbm_gbs", "algorithmic_bytes_per_launch": bytes_step}
     else:
         flops_step = 12 * w.D * pairs
-        value = world * flops_step / (ms_step / 1e3) / 1e12
+        value = whole_job_rate(flops_step, ms_step, world, 1e12)
         metric, unit = "attn-KL fwd+bwd TFLOP/s & ms (H32 D128 N64K causal), % bf16 TC peak", "TFLOP/s"
         dom = max(per_kernel, key=per_kernel.get)
         avg_ms = per_kernel[dom] / args.steps
