@@ -57,45 +57,63 @@ struct Smem {
 
 // dS for one thread's 64 columns; values are packed as bf16 pairs into pk[32].
 // KSTAT: X rows are keys and Y rows are queries (per-column row values).
+// Arithmetic on column pairs uses the packed fp32 instructions.
 template <int SETTING, bool KSTAT, bool MASKED>
 __device__ __forceinline__ void make_ds(uint32_t (&a0)[32], uint32_t (&a1)[32], uint32_t (&b0)[32],
                                         uint32_t (&b1)[32], uint32_t (&pk)[32], float c, const float* vals,
                                         float L1r, float L2r, float Gr, float KLr, int xidx, int y0, int nx, int ny,
                                         int off, int causal) {
+  const float2 cc = make_float2(c, c);
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
 #pragma unroll
     for (int i = 0; i < 32; i += 2) {
-      float ds[2];
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int col = h * 32 + i + e;
-        const float s1 = __uint_as_float(h == 0 ? a0[i + e] : a1[i + e]);
-        const float s2 = __uint_as_float(h == 0 ? b0[i + e] : b1[i + e]);
-        float L1 = L1r, L2 = L2r, G = Gr, KL = KLr;
-        if (KSTAT) {
-          L1 = vals[col];
-          L2 = vals[BY + col];
-          G = vals[2 * BY + col];
-          if (SETTING == 2) KL = vals[3 * BY + col];
-        }
-        bool keep = true;
-        if (MASKED) {
-          const int y = y0 + col;  // streamed index: key (dQ kernel) or query (dK kernel)
-          const int q = KSTAT ? y : xidx, k = KSTAT ? xidx : y;
-          const int nq = KSTAT ? ny : nx, nk = KSTAT ? nx : ny;
-          keep = q < nq && k < nk && (!causal || k <= q + off);
-        }
-        const float p1 = keep ? ex2(fmaf(s1, c, -L1)) : 0.f;
-        if (SETTING == 1) {
-          const float p2 = keep ? ex2(fmaf(s2, c, -L2)) : 0.f;
-          ds[e] = G * (p2 - p1);
-        } else {
-          const float r = kLn2 * fmaf(s1 - s2, c, L2 - L1);
-          ds[e] = G * p1 * (r - KL);
-        }
+      const int col = h * 32 + i;
+      const uint32_t* A = h == 0 ? a0 : a1;
+      const uint32_t* Bv = h == 0 ? b0 : b1;
+      const float2 s1 = make_float2(__uint_as_float(A[i]), __uint_as_float(A[i + 1]));
+      const float2 s2 = make_float2(__uint_as_float(Bv[i]), __uint_as_float(Bv[i + 1]));
+      float2 L1 = make_float2(L1r, L1r), L2 = make_float2(L2r, L2r), G = make_float2(Gr, Gr);
+      float2 KL = make_float2(KLr, KLr);
+      if (KSTAT) {
+        L1 = *reinterpret_cast<const float2*>(vals + col);
+        L2 = *reinterpret_cast<const float2*>(vals + BY + col);
+        G = *reinterpret_cast<const float2*>(vals + 2 * BY + col);
+        if (SETTING == 2) KL = *reinterpret_cast<const float2*>(vals + 3 * BY + col);
       }
-      pk[h * 16 + i / 2] = pack_bf16(ds[0], ds[1]);
+      const float2 x1 = ffma2(s1, cc, make_float2(-L1.x, -L1.y));
+      float2 p1 = make_float2(ex2(x1.x), ex2(x1.y));
+      if (MASKED) {
+        const int y = y0 + col;  // streamed index: key (dQ kernel) or query (dK kernel)
+        bool keep[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int q = KSTAT ? y + e : xidx, k = KSTAT ? xidx : y + e;
+          const int nq = KSTAT ? ny : nx, nk = KSTAT ? nx : ny;
+          keep[e] = q < nq && k < nk && (!causal || k <= q + off);
+        }
+        p1.x = keep[0] ? p1.x : 0.f;
+        p1.y = keep[1] ? p1.y : 0.f;
+        if (SETTING == 1) {
+          const float2 x2 = ffma2(s2, cc, make_float2(-L2.x, -L2.y));
+          const float2 p2 = make_float2(keep[0] ? ex2(x2.x) : 0.f, keep[1] ? ex2(x2.y) : 0.f);
+          const float2 ds = fmul2(G, fsub2(p2, p1));
+          pk[col / 2] = pack_bf16(ds.x, ds.y);
+          continue;
+        }
+      } else if (SETTING == 1) {
+        const float2 x2 = ffma2(s2, cc, make_float2(-L2.x, -L2.y));
+        const float2 p2 = make_float2(ex2(x2.x), ex2(x2.y));
+        const float2 ds = fmul2(G, fsub2(p2, p1));
+        pk[col / 2] = pack_bf16(ds.x, ds.y);
+        continue;
+      }
+      if (SETTING == 2) {
+        // r = ln2 ((s1 - s2) c - (L1 - L2));  dS1 = g p1 (r - KL)
+        const float2 r = fmul2(make_float2(kLn2, kLn2), ffma2(fsub2(s1, s2), cc, fsub2(L2, L1)));
+        const float2 ds = fmul2(fmul2(G, p1), fsub2(r, KL));
+        pk[col / 2] = pack_bf16(ds.x, ds.y);
+      }
     }
   }
 }

@@ -62,11 +62,15 @@ struct Row5 {
   float m1, m2, l1, l2, acc;
 };
 
+// Masked logits are set to this finite sentinel (not -inf) in both S1 and S2:
+// their weight 2^(c*sentinel - m) is exactly 0 and their difference S1 - S2 is
+// exactly 0, so the packed arithmetic below needs no per-element selects.
+constexpr float kMaskedLogit = -1.0e30f;
+
 template <bool MASKED>
 __device__ __forceinline__ void online_update(Row5& st, uint32_t (&a0)[32], uint32_t (&a1)[32], uint32_t (&b0)[32],
                                               uint32_t (&b1)[32], float c, int key0, int row_lim, int nk) {
   // a*: raw S1 = q1.k1 (64 columns), b*: raw S2; key0 = key index of column 0
-  float mx1 = kNegInf, mx2 = kNegInf;
   if (MASKED) {
 #pragma unroll
     for (int i = 0; i < 64; ++i) {
@@ -75,17 +79,18 @@ __device__ __forceinline__ void online_update(Row5& st, uint32_t (&a0)[32], uint
       uint32_t& s1 = i < 32 ? a0[i] : a1[i - 32];
       uint32_t& s2 = i < 32 ? b0[i] : b1[i - 32];
       if (!keep) {
-        s1 = __float_as_uint(kNegInf);
-        s2 = __float_as_uint(kNegInf);
+        s1 = __float_as_uint(kMaskedLogit);
+        s2 = __float_as_uint(kMaskedLogit);
       }
     }
   }
+  float mx1 = kMaskedLogit, mx2 = kMaskedLogit;
 #pragma unroll
   for (int i = 0; i < 32; ++i) {
-    mx1 = fmaxf(mx1, fmaxf(__uint_as_float(a0[i]), __uint_as_float(a1[i])));
-    mx2 = fmaxf(mx2, fmaxf(__uint_as_float(b0[i]), __uint_as_float(b1[i])));
+    mx1 = fmax3(mx1, __uint_as_float(a0[i]), __uint_as_float(a1[i]));
+    mx2 = fmax3(mx2, __uint_as_float(b0[i]), __uint_as_float(b1[i]));
   }
-  if (mx1 == kNegInf) return;  // every column of this tile is masked for this row
+  if (MASKED && mx1 == kMaskedLogit) return;  // every column of this tile is masked for this row
   const float t1 = mx1 * c, t2 = mx2 * c;
   if (t1 > st.m1 + kLazy) {
     const float al = ex2(st.m1 - t1);
@@ -98,30 +103,28 @@ __device__ __forceinline__ void online_update(Row5& st, uint32_t (&a0)[32], uint
     st.l2 *= al;
     st.m2 = t2;
   }
-  const float n1 = -st.m1, n2 = -st.m2;
-  float l1a = 0.f, l1b = 0.f, l2a = 0.f, l2b = 0.f, acca = 0.f, accb = 0.f;
+  const float2 cc = make_float2(c, c);
+  const float2 n1 = make_float2(-st.m1, -st.m1), n2 = make_float2(-st.m2, -st.m2);
+  float2 l1 = make_float2(0.f, 0.f), l2 = make_float2(0.f, 0.f), acc = make_float2(0.f, 0.f);
 #pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    const float s1x = __uint_as_float(a0[i]), s1y = __uint_as_float(a1[i]);
-    const float s2x = __uint_as_float(b0[i]), s2y = __uint_as_float(b1[i]);
-    const float p1x = ex2(fmaf(s1x, c, n1)), p1y = ex2(fmaf(s1y, c, n1));
-    const float p2x = ex2(fmaf(s2x, c, n2)), p2y = ex2(fmaf(s2y, c, n2));
-    l1a += p1x;
-    l1b += p1y;
-    l2a += p2x;
-    l2b += p2y;
-    if (MASKED) {
-      // masked columns have p1 = 0 but s1 - s2 = -inf - -inf: keep them out
-      acca += p1x > 0.f ? p1x * (s1x - s2x) : 0.f;
-      accb += p1y > 0.f ? p1y * (s1y - s2y) : 0.f;
-    } else {
-      acca = fmaf(p1x, s1x - s2x, acca);
-      accb = fmaf(p1y, s1y - s2y, accb);
+  for (int h = 0; h < 2; ++h) {
+#pragma unroll
+    for (int i = 0; i < 32; i += 2) {
+      const uint32_t* A = h == 0 ? a0 : a1;
+      const uint32_t* Bv = h == 0 ? b0 : b1;
+      const float2 s1 = make_float2(__uint_as_float(A[i]), __uint_as_float(A[i + 1]));
+      const float2 s2 = make_float2(__uint_as_float(Bv[i]), __uint_as_float(Bv[i + 1]));
+      const float2 x1 = ffma2(s1, cc, n1), x2 = ffma2(s2, cc, n2);
+      const float2 p1 = make_float2(ex2(x1.x), ex2(x1.y));
+      const float2 p2 = make_float2(ex2(x2.x), ex2(x2.y));
+      l1 = fadd2(l1, p1);
+      l2 = fadd2(l2, p2);
+      acc = ffma2(p1, fsub2(s1, s2), acc);
     }
   }
-  st.l1 += l1a + l1b;
-  st.l2 += l2a + l2b;
-  st.acc += acca + accb;
+  st.l1 += l1.x + l1.y;
+  st.l2 += l2.x + l2.y;
+  st.acc += acc.x + acc.y;
 }
 
 template <int D>
