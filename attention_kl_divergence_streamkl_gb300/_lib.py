@@ -46,7 +46,7 @@ SIGNATURES = {
     "streamkl_fwd_splitk_plan": (_I, [Shape, _I, ctypes.POINTER(_I)]),
     "streamkl_fwd_splitk_noalloc": (_I, [_P, _P, _P, _P, Shape, _I, _F, _F, _F, _S]),
     "streamkl_bwd_workspace": (_I, [Shape, _I, ctypes.POINTER(_SZ)]),
-    "streamkl_bwd_select": (_I, [Shape, _SZ]),
+    "streamkl_bwd_select": (_I, [Shape, _SZ, _I]),
     "streamkl_bwd_s1": (_I, [_P, _P, _P, _P, Shape, _F, _F, _F, _P, _P, _I, _P, _SZ, _S]),
     "streamkl_bwd_s2": (_I, [_P, _P, _P, _P, Shape, _F, _F, _F, _F, _P, _P, _I, _P, _SZ, _S]),
     "streamkl_status_string": (ctypes.c_char_p, [_I]),
@@ -167,8 +167,8 @@ def fwd_splitk(q1, k1, q2, k2, scale=None, causal=False, num_splits=0):
     return _back((kl, l1, l2), host)
 
 
-def bwd_select(B, H, NQ, NK, D, l2_bytes, causal=False) -> int:
-    return lib().streamkl_bwd_select(make_shape(B, H, NQ, NK, D, None, causal), int(l2_bytes))
+def bwd_select(B, H, NQ, NK, D, l2_bytes, num_sms, causal=False) -> int:
+    return lib().streamkl_bwd_select(make_shape(B, H, NQ, NK, D, None, causal), int(l2_bytes), int(num_sms))
 
 
 def bwd_workspace_bytes(B, H, NQ, NK, D, bwd_mode=BWD_AUTO, causal=False) -> int:

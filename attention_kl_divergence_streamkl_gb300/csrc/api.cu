@@ -74,9 +74,21 @@ streamkl_status from_cuda(cudaError_t e) { return e == cudaSuccess ? STREAMKL_OK
 
 size_t dq_acc_bytes(const Problem& p) { return (size_t)p.BH * p.NQ * p.D * sizeof(float); }
 
-int resolve_bwd_mode(const Problem& p, int mode, size_t l2_bytes) {
+// The fused path adds dQ partials into the fp32 buffer with atomics; they stay
+// cheap while the rows being accumulated stay in L2.  Its blocks run head by
+// head (all key tiles of one (b, h) before the next), so the live part of the
+// buffer is the dQ rows of the heads that are in flight at once: one head's
+// N_Q x D fp32 rows times the heads a full wave of blocks spans.
+size_t live_dq_bytes(const Problem& p, int num_sms) {
+  const long long key_tiles = (p.NK + 127) / 128;  // blocks per head
+  const long long heads_in_flight = (num_sms + key_tiles - 1) / key_tiles + 1;
+  const long long heads = heads_in_flight < p.BH ? heads_in_flight : p.BH;
+  return (size_t)p.NQ * p.D * sizeof(float) * (size_t)heads;
+}
+
+int resolve_bwd_mode(const Problem& p, int mode, size_t l2_bytes, int num_sms) {
   if (mode == STREAMKL_BWD_FUSED || mode == STREAMKL_BWD_SEPARATE) return mode;
-  return dq_acc_bytes(p) <= l2_bytes ? STREAMKL_BWD_FUSED : STREAMKL_BWD_SEPARATE;
+  return live_dq_bytes(p, num_sms) <= l2_bytes ? STREAMKL_BWD_FUSED : STREAMKL_BWD_SEPARATE;
 }
 
 streamkl_status device_l2_bytes(size_t* out) {
@@ -221,10 +233,10 @@ streamkl_status streamkl_fwd_splitk_noalloc(const void* q1, const void* k1, cons
                                  static_cast<cudaStream_t>(stream)));
 }
 
-int streamkl_bwd_select(streamkl_shape s, size_t l2_bytes) {
+int streamkl_bwd_select(streamkl_shape s, size_t l2_bytes, int num_sms) {
   Problem p;
-  if (validate(s, &p) != STREAMKL_OK) return 0;
-  return resolve_bwd_mode(p, STREAMKL_BWD_AUTO, l2_bytes);
+  if (validate(s, &p) != STREAMKL_OK || num_sms <= 0) return 0;
+  return resolve_bwd_mode(p, STREAMKL_BWD_AUTO, l2_bytes, num_sms);
 }
 
 streamkl_status streamkl_bwd_workspace(streamkl_shape s, int bwd_mode, size_t* bytes) {
@@ -234,8 +246,9 @@ streamkl_status streamkl_bwd_workspace(streamkl_shape s, int bwd_mode, size_t* b
   if (!bytes || bwd_mode < 0 || bwd_mode > STREAMKL_BWD_DK_ONLY) return STREAMKL_ERR_INVALID;
   if (bwd_mode == STREAMKL_BWD_AUTO) {
     size_t l2 = 0;
-    if ((v = device_l2_bytes(&l2)) != STREAMKL_OK) return v;
-    bwd_mode = resolve_bwd_mode(p, bwd_mode, l2);
+    int sms = 0;
+    if ((v = device_l2_bytes(&l2)) != STREAMKL_OK || (v = device_sms(&sms)) != STREAMKL_OK) return v;
+    bwd_mode = resolve_bwd_mode(p, bwd_mode, l2, sms);
   }
   *bytes = bwd_mode == STREAMKL_BWD_FUSED ? dq_acc_bytes(p) : 0;
   return STREAMKL_OK;
@@ -263,8 +276,9 @@ static streamkl_status bwd_common(int setting, const void* q1, const void* k1, c
   if (setting == 2 && !rows_ok(kl)) return STREAMKL_ERR_INVALID;
   if (bwd_mode == STREAMKL_BWD_AUTO) {
     size_t l2 = 0;
-    if ((v = device_l2_bytes(&l2)) != STREAMKL_OK) return v;
-    bwd_mode = resolve_bwd_mode(p, bwd_mode, l2);
+    int sms = 0;
+    if ((v = device_l2_bytes(&l2)) != STREAMKL_OK || (v = device_sms(&sms)) != STREAMKL_OK) return v;
+    bwd_mode = resolve_bwd_mode(p, bwd_mode, l2, sms);
   }
   if (bwd_mode == STREAMKL_BWD_FUSED &&
       (!workspace || !aligned16(workspace) || workspace_bytes < dq_acc_bytes(p)))

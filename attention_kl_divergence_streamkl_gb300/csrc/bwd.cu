@@ -1,284 +1,398 @@
-// Recompute-based attention-KL backward, both settings.
+// Fused attention-KL backward on the 5th-generation tensor cores.
 //
 // StreamKL technical summary (gist.science/ja/paper/2606.20005), section 手法 2
-// "recompute strategy": only KL, LSE1 and LSE2 are kept from the forward; the
-// backward rebuilds P_t = exp(S_t - LSE_t) tile by tile from Q, K and the saved
-// LSE.  Setting 1 holds P1 fixed and optimises the student side (Q2, K2);
-// setting 2 holds P2 fixed and optimises Q1, K1.  Section 手法 3 "numerical
-// stability": the setting-2 log ratio is formed from the logits and the saved
-// LSEs, never from log of probabilities.  The gradient of L = sum_i g_i KL_i
-// with respect to the logits is (derived by the chain rule):
-//     setting 1:  dS2 = g_i (P2 - P1)
-//     setting 2:  dS1 = g_i P1 (r - KL_i),  r = (S1 - LSE1) - (S2 - LSE2)
-// and for the optimised pair dQ = scale dS K, dK = scale dS^T Q.
+// "kernel fusion": each (query tile, key tile) pair is visited exactly once; dK
+// accumulates along the queries inside the block and dQ, which accumulates
+// along the keys, is added into an fp32 buffer with atomics -- the path the
+// library takes while that buffer fits in L2.  Gradient formulas as in
+// bwd_tc.cu (setting 1: dS2 = g (P2 - P1); setting 2: dS1 = g P1 (r - KL)).
 //
-// This file holds the fused path (section 手法 2 "kernel fusion"): each
-// (query tile, key tile) pair is visited once from a key-stationary block, dK
-// accumulates in registers and the dQ contribution is added into an fp32
-// buffer with vector atomics, which the library uses while that buffer fits in
-// L2.  The separate path (a query-stationary dQ kernel and a key-stationary dK
-// kernel on tcgen05) is in bwd_tc.cu.
+// Block = one 128-key tile (stationary K1, K2 in smem; keys on the 128 TMEM
+// lanes), streaming 64-query tiles Y:
+//   S1^T = K1 Q1^T, S2^T = K2 Q2^T    SS, M = 128 keys, N = 64 queries (double-buffered in TMEM)
+//   dS^T from S^T and the per-query LSE1, LSE2, g, KL of the tile
+//   dK  += dS^T Q_opt                 TS: A = dS^T packed bf16 over S1^T's columns, B = Q_opt MN-major
+//   dQp^T = K_opt^T dS                SS: A = K_opt read MN-major (M = D on lanes), B = dS^T in smem
+//   dq_acc[q, d] += dQp^T[d, q]       one warp adds 32 consecutive d of one query row (128 B) per red
+// TMEM: S^T buffer b at [128b, 128b + 128) (S1^T then S2^T, 64 columns each),
+// dK at [256, 256 + D), dQp^T buffer b at [384 + 64b, 448 + 64b).
+//   warp 12     TMA producer; its 32 lanes also stage the per-query values
+//   warp 13     TMEM owner and MMA issuer (S(j) issued before dK/dQp of tile j-1)
+//   warps 0-7   dS warps: thread = key row, group g = query columns [32g, 32g + 32)
+//   warps 8-11  dQ warps: thread = column d of dQp^T, reduce-add into dq_acc
 #include "common.cuh"
 #include "kernels.h"
+#include "tc.cuh"
 
 namespace skl {
 namespace {
 
-constexpr int CONSUMERS = 8;
-constexpr int THREADS = (CONSUMERS + 1) * 32;
-constexpr int STAGES = 2;
+constexpr int BK = 128;  // keys per block (M of the S and dK MMAs)
+constexpr int BQ = 64;   // queries per step
+constexpr int STAGES = 3;
+constexpr int DS_WARPS = 8;
+constexpr int DQ_WARP0 = 8;
+constexpr int PRODUCER_WARP = 12;
+constexpr int MMA_WARP = 13;
+constexpr int THREADS = 14 * 32;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColDK = 256, kColDQ = 384;
 
-// ============================================================================
-// dK kernel (and fused dK + dQ-atomics): one block per (b*h, 128-key tile),
-// streams 64-row query tiles together with their LSE1, LSE2, g, KL values.
-// ============================================================================
-constexpr int KBK = 128;
-constexpr int KBQ = 64;
-
-template <int D, bool FUSED>
-struct DkSmem {
-  static constexpr int K_BYTES = KBK * D * 2;
-  static constexpr int Q_BYTES = KBQ * D * 2;
-  static constexpr int V_BYTES = 4 * KBQ * 4;  // lse1', lse2', g, kl per query row
+template <int D>
+struct Smem {
+  static constexpr int KT = BK * D * 2;   // one 128-key tile
+  static constexpr int QT = BQ * D * 2;   // one 64-query tile (D/64 halves of 8 KiB)
   static constexpr int OFF_K1 = 0;
-  static constexpr int OFF_K2 = K_BYTES;
-  static constexpr int OFF_STAGE = 2 * K_BYTES;
-  static constexpr int STAGE_BYTES = 2 * Q_BYTES + V_BYTES;  // every term a multiple of 1024
-  static constexpr int OFF_DS = OFF_STAGE + STAGES * STAGE_BYTES;
-  static constexpr int DS_BYTES = FUSED ? KBK * KBQ * 2 : 0;  // bf16 dS^T [128 keys][64 queries]
-  static constexpr int OFF_BAR = OFF_DS + 2 * DS_BYTES;
-  static constexpr int BYTES = OFF_BAR + 8 + 16 * STAGES + 16 + 1024;
+  static constexpr int OFF_K2 = KT;
+  static constexpr int OFF_Q = 2 * KT;  // stage s: Q1, Q2
+  static constexpr int STAGE = 2 * QT;
+  static constexpr int OFF_DS = OFF_Q + STAGES * STAGE;  // [2][128 keys][64 queries] bf16, 16 KiB each
+  static constexpr int DS_BYTES = BK * BQ * 2;
+  static constexpr int OFF_VALS = OFF_DS + 2 * DS_BYTES;  // [STAGES][4][64] fp32
+  static constexpr int OFF_BAR = OFF_VALS + STAGES * 4 * BQ * 4;
+  // k_full, y_full[3], y_empty[3], s_full[2], s_free[2], ds_full[2], ds_free[2], dq_full[2], dq_free[2], slot, abort
+  static constexpr int BYTES = OFF_BAR + 8 * 19 + 16 + 1024;
 };
 
-template <int D, int SETTING, bool FUSED>
+template <int SETTING, bool MASKED>
+__device__ __forceinline__ void make_dst(const uint32_t (&a)[32], const uint32_t (&b)[32], uint32_t (&pk)[16],
+                                         float c, const float* vals, int key, int q0, int nq, int nk, int off,
+                                         int causal) {
+  // thread = one key; 32 query columns q0 .. q0 + 31 with their values in vals[*][0..31]
+#pragma unroll
+  for (int i = 0; i < 32; i += 2) {
+    const float2 s1 = make_float2(__uint_as_float(a[i]), __uint_as_float(a[i + 1]));
+    const float2 s2 = make_float2(__uint_as_float(b[i]), __uint_as_float(b[i + 1]));
+    const float2 L1 = make_float2(vals[i], vals[i + 1]);
+    const float2 L2 = make_float2(vals[BQ + i], vals[BQ + i + 1]);
+    const float2 G = make_float2(vals[2 * BQ + i], vals[2 * BQ + i + 1]);
+    const float2 cc = make_float2(c, c);
+    const float2 x1 = ffma2(s1, cc, make_float2(-L1.x, -L1.y));
+    float2 p1 = make_float2(ex2(x1.x), ex2(x1.y));
+    float2 ds;
+    if (SETTING == 1) {
+      const float2 x2 = ffma2(s2, cc, make_float2(-L2.x, -L2.y));
+      float2 p2 = make_float2(ex2(x2.x), ex2(x2.y));
+      if (MASKED) {
+        const int q = q0 + i;
+        const bool k0 = q < nq && key < nk && (!causal || key <= q + off);
+        const bool k1 = q + 1 < nq && key < nk && (!causal || key <= q + 1 + off);
+        p1.x = k0 ? p1.x : 0.f;
+        p1.y = k1 ? p1.y : 0.f;
+        p2.x = k0 ? p2.x : 0.f;
+        p2.y = k1 ? p2.y : 0.f;
+      }
+      ds = fmul2(G, fsub2(p2, p1));
+    } else {
+      if (MASKED) {
+        const int q = q0 + i;
+        p1.x = (q < nq && key < nk && (!causal || key <= q + off)) ? p1.x : 0.f;
+        p1.y = (q + 1 < nq && key < nk && (!causal || key <= q + 1 + off)) ? p1.y : 0.f;
+      }
+      const float2 KL = make_float2(vals[3 * BQ + i], vals[3 * BQ + i + 1]);
+      // r = ln2 ((s1 - s2) c - (L1 - L2))
+      const float2 r = fmul2(make_float2(kLn2, kLn2), ffma2(fsub2(s1, s2), cc, fsub2(L2, L1)));
+      ds = fmul2(fmul2(G, p1), fsub2(r, KL));
+    }
+    pk[i / 2] = pack_bf16(ds.x, ds.y);
+  }
+}
+
+template <int D, int SETTING>
 __global__ void __launch_bounds__(THREADS, 1)
-    bwd_dk_kernel(const Problem p, const float* __restrict__ lse1, const float* __restrict__ lse2,
-                  const float* __restrict__ klv, const float* __restrict__ gv, __nv_bfloat16* __restrict__ dk_out,
-                  float* __restrict__ dq_acc, int* status, const __grid_constant__ CUtensorMap mq1,
-                  const __grid_constant__ CUtensorMap mk1, const __grid_constant__ CUtensorMap mq2,
-                  const __grid_constant__ CUtensorMap mk2) {
-  using L = DkSmem<D, FUSED>;
+    bwd_fused_tc_kernel(const Problem p, const float* __restrict__ lse1, const float* __restrict__ lse2,
+                        const float* __restrict__ klv, const float* __restrict__ gv,
+                        __nv_bfloat16* __restrict__ dk_out, float* __restrict__ dq_acc, int* status,
+                        const __grid_constant__ CUtensorMap mk1, const __grid_constant__ CUtensorMap mk2,
+                        const __grid_constant__ CUtensorMap mq1, const __grid_constant__ CUtensorMap mq2) {
+  using L = Smem<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   const uint32_t sb = smem_u32(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int bh = blockIdx.x;
-  const int kt = blockIdx.y;
-  const int kb0 = kt * KBK;
-  const int n_qt = (p.NQ + KBQ - 1) / KBQ;
-  const int qs = p.causal ? max(0, kb0 - p.off) / KBQ : 0;
-  const int n_it = n_qt - qs;
+  const int n_kt = (p.NK + BK - 1) / BK;
+  const int bh = (int)(blockIdx.x / n_kt);  // heads in order (their dq_acc rows stay in L2), ...
+  const int kt = (int)(blockIdx.x % n_kt);  // ... and within a head the longest (first) key tiles first
+  const int k0 = kt * BK;
+  const int q_begin = p.causal ? max(0, k0 - p.off) / BQ * BQ : 0;
+  const int n_yt = (p.NQ - q_begin + BQ - 1) / BQ;
 
-  const uint32_t bar_k = sb + L::OFF_BAR;
-  const uint32_t bar_full = bar_k + 8;
-  const uint32_t bar_empty = bar_full + 8 * STAGES;
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_BAR + 8 + 16 * STAGES);
+  const uint32_t bar = sb + L::OFF_BAR;
+  const uint32_t k_full = bar, y_full = bar + 8, y_empty = bar + 32, s_full = bar + 56, s_free = bar + 72,
+                 ds_full = bar + 88, ds_free = bar + 104, dq_full = bar + 120, dq_free = bar + 136,
+                 slot = bar + 152;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_BAR + 156);
+
   if (threadIdx.x == 0) {
-    mbar_init(bar_k, 1);
+    mbar_init(k_full, 1);
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(bar_full + 8 * s, 32);  // 32 producer lanes store row values; lane 0 also posts the TMA bytes
-      mbar_init(bar_empty + 8 * s, CONSUMERS);
+      mbar_init(y_full + 8 * s, 32);
+      mbar_init(y_empty + 8 * s, 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(s_full + 8 * b, 1);
+      mbar_init(s_free + 8 * b, DS_WARPS);
+      mbar_init(ds_full + 8 * b, DS_WARPS);
+      mbar_init(ds_free + 8 * b, 1);
+      mbar_init(dq_full + 8 * b, 1);
+      mbar_init(dq_free + 8 * b, 4);
     }
     *abort_flag = 0;
     fence_mbar_init();
   }
+  if (warp == MMA_WARP) {
+    tmem_alloc(slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
   __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::OFF_BAR + 152);
 
-  if (warp == CONSUMERS) {
-    // ------------------------------------------------------------ producer warp
+  if (warp == PRODUCER_WARP) {
+    // ------------------------------------------------------------------ producer
     if (lane == 0) {
-      mbar_arrive_expect_tx(bar_k, 2 * L::K_BYTES);
+      mbar_arrive_expect_tx(k_full, 2 * L::KT);
 #pragma unroll
       for (int h = 0; h < D / 64; ++h) {
-        tma_load_3d(sb + L::OFF_K1 + h * KBK * 128, &mk1, bar_k, h * 64, kb0, bh);
-        tma_load_3d(sb + L::OFF_K2 + h * KBK * 128, &mk2, bar_k, h * 64, kb0, bh);
+        tma_load_3d(sb + L::OFF_K1 + h * BK * 128, &mk1, k_full, h * 64, k0, bh);
+        tma_load_3d(sb + L::OFF_K2 + h * BK * 128, &mk2, k_full, h * 64, k0, bh);
       }
     }
     int issued = 0;
-    for (int it = 0; it < n_it; ++it) {
-      const int s = it % STAGES;
-      if (it >= STAGES && !mbar_wait(bar_empty + 8 * s, ((it / STAGES) - 1) & 1, status, abort_flag)) break;
-      const int q0 = (qs + it) * KBQ;
-      const uint32_t st_base = sb + L::OFF_STAGE + s * L::STAGE_BYTES;
+    for (int j = 0; j < n_yt; ++j) {
+      const int s = j % STAGES;
+      const bool free_ok = j < STAGES || mbar_wait(y_empty + 8 * s, ((j / STAGES) - 1) & 1, status, abort_flag);
+      __syncwarp();
+      if (!free_ok) break;
+      const int q0 = q_begin + j * BQ;
+      const uint32_t qb = sb + L::OFF_Q + s * L::STAGE;
       if (lane == 0) {
-        mbar_expect_tx(bar_full + 8 * s, 2 * L::Q_BYTES);
+        mbar_expect_tx(y_full + 8 * s, 2 * L::QT);
 #pragma unroll
         for (int h = 0; h < D / 64; ++h) {
-          tma_load_3d(st_base + h * KBQ * 128, &mq1, bar_full + 8 * s, h * 64, q0, bh);
-          tma_load_3d(st_base + L::Q_BYTES + h * KBQ * 128, &mq2, bar_full + 8 * s, h * 64, q0, bh);
+          tma_load_3d(qb + h * BQ * 128, &mq1, y_full + 8 * s, h * 64, q0, bh);
+          tma_load_3d(qb + L::QT + h * BQ * 128, &mq2, y_full + 8 * s, h * 64, q0, bh);
         }
       }
-      float* vals = reinterpret_cast<float*>(smem + L::OFF_STAGE + s * L::STAGE_BYTES + 2 * L::Q_BYTES);
+      float* vals = reinterpret_cast<float*>(smem + L::OFF_VALS + s * 4 * BQ * 4);
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        const int qi = lane + half * 32;
-        const int q = q0 + qi;
+      for (int k = 0; k < BQ / 32; ++k) {
+        const int qi = lane + 32 * k, q = q0 + qi;
         const bool in = q < p.NQ;
         const size_t o = (size_t)bh * p.NQ + q;
         vals[qi] = in ? lse1[o] * kLog2e : 0.f;
-        vals[KBQ + qi] = in ? lse2[o] * kLog2e : 0.f;
-        vals[2 * KBQ + qi] = in ? gv[o] : 0.f;
-        vals[3 * KBQ + qi] = (SETTING == 2 && in) ? klv[o] : 0.f;
+        vals[BQ + qi] = in ? lse2[o] * kLog2e : 0.f;
+        vals[2 * BQ + qi] = in ? gv[o] : 0.f;
+        vals[3 * BQ + qi] = (SETTING == 2 && in) ? klv[o] : 0.f;
       }
-      mbar_arrive(bar_full + 8 * s);
-      issued = it + 1;
+      mbar_arrive(y_full + 8 * s);
+      issued = j + 1;
     }
     if (lane == 0) {
-      mbar_drain(bar_k, 0, status);
-      for (int it = max(0, issued - STAGES); it < issued; ++it)
-        mbar_drain(bar_full + 8 * (it % STAGES), (it / STAGES) & 1, status);
-    }
-    return;
-  }
-
-  // -------------------------------------------------------------- consumers
-  const int g = lane >> 2, t = lane & 3;
-  const float c = p.c;
-  const int key0 = kb0 + warp * 16 + g;  // this thread's keys: key0, key0 + 8
-  float dk[D / 8][4];
-#pragma unroll
-  for (int n = 0; n < D / 8; ++n)
-#pragma unroll
-    for (int j = 0; j < 4; ++j) dk[n][j] = 0.f;
-
-  bool ok = mbar_wait(bar_k, 0, status, abort_flag);
-  const int arow = warp * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-  const int acol = lane >> 4;
-  const int brow = (lane & 7) + (lane >> 4) * 8;
-  const int bcol = (lane >> 3) & 1;
-  const int trow = (lane & 7) + ((lane >> 3) & 1) * 8;
-  const int tcol = lane >> 4;
-
-  for (int it = 0; ok && it < n_it; ++it) {
-    const int s = it % STAGES;
-    if (!mbar_wait(bar_full + 8 * s, (it / STAGES) & 1, status, abort_flag)) {
-      ok = false;
-      break;
-    }
-    const int q0 = (qs + it) * KBQ;
-    const uint32_t qb1 = sb + L::OFF_STAGE + s * L::STAGE_BYTES;
-    const uint32_t qb2 = qb1 + L::Q_BYTES;
-    const float* vals = reinterpret_cast<const float*>(smem + L::OFF_STAGE + s * L::STAGE_BYTES + 2 * L::Q_BYTES);
-
-    // S^T = K Q^T for this warp's 16 keys and the 64 queries of the tile
-    float s1[8][4], s2[8][4];
-#pragma unroll
-    for (int n = 0; n < 8; ++n)
-#pragma unroll
-      for (int j = 0; j < 4; ++j) s1[n][j] = s2[n][j] = 0.f;
-#pragma unroll
-    for (int ks = 0; ks < D / 16; ++ks) {
-      uint32_t a1[4], a2[4];
-      ldsm_x4(sw128<KBK>(sb + L::OFF_K1, arow, 2 * ks + acol), a1);
-      ldsm_x4(sw128<KBK>(sb + L::OFF_K2, arow, 2 * ks + acol), a2);
-#pragma unroll
-      for (int np = 0; np < 4; ++np) {
-        uint32_t b[4];
-        ldsm_x4(sw128<KBQ>(qb1, np * 16 + brow, 2 * ks + bcol), b);
-        mma16816(s1[2 * np], a1, b[0], b[1]);
-        mma16816(s1[2 * np + 1], a1, b[2], b[3]);
-        ldsm_x4(sw128<KBQ>(qb2, np * 16 + brow, 2 * ks + bcol), b);
-        mma16816(s2[2 * np], a2, b[0], b[1]);
-        mma16816(s2[2 * np + 1], a2, b[2], b[3]);
-      }
-    }
-    const bool need_mask =
-        (q0 + KBQ > p.NQ) || (kb0 + KBK > p.NK) || (p.causal && kb0 + KBK - 1 > q0 + p.off);
-    uint32_t af[4][4];
-#pragma unroll
-    for (int n = 0; n < 8; ++n) {
-      float ds[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int key = key0 + (j >> 1) * 8;
-        const int qi = n * 8 + 2 * t + (j & 1);
-        const int q = q0 + qi;
-        const bool keep = !need_mask || (q < p.NQ && key < p.NK && (!p.causal || key <= q + p.off));
-        const float L1 = vals[qi], L2 = vals[KBQ + qi], G = vals[2 * KBQ + qi];
-        const float p1 = keep ? ex2(fmaf(s1[n][j], c, -L1)) : 0.f;
-        if (SETTING == 1) {
-          const float p2 = keep ? ex2(fmaf(s2[n][j], c, -L2)) : 0.f;
-          ds[j] = G * (p2 - p1);
-        } else {
-          const float r = kLn2 * fmaf(s1[n][j] - s2[n][j], c, L2 - L1);
-          ds[j] = G * p1 * (r - vals[3 * KBQ + qi]);
-        }
-      }
-      af[n >> 1][2 * (n & 1) + 0] = pack_bf16(ds[0], ds[1]);
-      af[n >> 1][2 * (n & 1) + 1] = pack_bf16(ds[2], ds[3]);
-    }
-    const uint32_t dsb = sb + L::OFF_DS + (it & 1) * L::DS_BYTES;
-    if (FUSED) {
-      // dS^T (keys x queries) to shared memory for the dQ contraction
-#pragma unroll
-      for (int n = 0; n < 8; ++n) {
-        const uint32_t a0 = sw128<KBK>(dsb, warp * 16 + g, n) + 4 * t;
-        const uint32_t a8 = sw128<KBK>(dsb, warp * 16 + g + 8, n) + 4 * t;
-        asm volatile("st.shared.u32 [%0], %1;" ::"r"(a0), "r"(af[n >> 1][2 * (n & 1)]) : "memory");
-        asm volatile("st.shared.u32 [%0], %1;" ::"r"(a8), "r"(af[n >> 1][2 * (n & 1) + 1]) : "memory");
-      }
-    }
-    // dK += dS^T Q_opt
-    const uint32_t qopt = SETTING == 1 ? qb2 : qb1;
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-#pragma unroll
-      for (int np = 0; np < D / 16; ++np) {
-        uint32_t b[4];
-        ldsm_x4_t(sw128<KBQ>(qopt, kk * 16 + trow, 2 * np + tcol), b);
-        mma16816(dk[2 * np], af[kk], b[0], b[1]);
-        mma16816(dk[2 * np + 1], af[kk], b[2], b[3]);
-      }
+      mbar_drain(k_full, 0, status);
+      for (int j = max(0, issued - STAGES); j < issued; ++j)
+        mbar_drain(y_full + 8 * (j % STAGES), (j / STAGES) & 1, status);
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(bar_empty + 8 * s);
-
-    if (FUSED) {
-      // dQ partial = dS (64 queries x 128 keys) K_opt (128 keys x D): each warp
-      // owns 16 queries x D/2 columns; results go to the fp32 buffer atomically.
-      named_bar_sync(1, CONSUMERS * 32);
-      const int qg = warp >> 1, dh = warp & 1;
+  } else if (warp == MMA_WARP) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t id_s = idesc_bf16(BK, BQ, false, false);
+      constexpr uint32_t id_dk = idesc_bf16(BK, D, false, true);
+      constexpr uint32_t id_dq = idesc_bf16(128, BQ, true, true);
       const uint32_t kopt = sb + (SETTING == 1 ? L::OFF_K2 : L::OFF_K1);
-      float pq[D / 16][4];
+      bool ok = mbar_wait(k_full, 0, status, abort_flag);
+      for (int j = 0; ok && j <= n_yt; ++j) {
+        if (j < n_yt) {
+          const int s = j % STAGES, b = j & 1;
+          if (!mbar_wait(y_full + 8 * s, (j / STAGES) & 1, status, abort_flag)) break;
+          if (j >= 2 && !mbar_wait(s_free + 8 * b, ((j >> 1) - 1) & 1, status, abort_flag)) break;
+          tc_fence_after();
+          const uint32_t q1 = sb + L::OFF_Q + s * L::STAGE, q2 = q1 + L::QT;
 #pragma unroll
-      for (int n = 0; n < D / 16; ++n)
+          for (int ks = 0; ks < D / 16; ++ks) {
+            const uint32_t ka = (ks >> 2) * (BK * 128) + (ks & 3) * 32;  // 128-key tile halves
+            const uint32_t qa = (ks >> 2) * (BQ * 128) + (ks & 3) * 32;  // 64-query tile halves
+            mma_ss(tmem + 128 * b, sdesc_sw128(sb + L::OFF_K1 + ka, 0, 1024), sdesc_sw128(q1 + qa, 0, 1024), id_s,
+                   ks > 0);
+          }
 #pragma unroll
-        for (int j = 0; j < 4; ++j) pq[n][j] = 0.f;
+          for (int ks = 0; ks < D / 16; ++ks) {
+            const uint32_t ka = (ks >> 2) * (BK * 128) + (ks & 3) * 32;
+            const uint32_t qa = (ks >> 2) * (BQ * 128) + (ks & 3) * 32;
+            mma_ss(tmem + 128 * b + 64, sdesc_sw128(sb + L::OFF_K2 + ka, 0, 1024), sdesc_sw128(q2 + qa, 0, 1024),
+                   id_s, ks > 0);
+          }
+          mma_commit(s_full + 8 * b);
+        }
+        if (j >= 1) {
+          const int jj = j - 1, b = jj & 1, s = jj % STAGES;
+          if (!mbar_wait(ds_full + 8 * b, (jj >> 1) & 1, status, abort_flag)) break;
+          if (jj >= 2 && !mbar_wait(dq_free + 8 * b, ((jj >> 1) - 1) & 1, status, abort_flag)) break;
+          tc_fence_after();
+          // dK += dS^T Q_opt: A = packed dS^T in TMEM (query k-steps 0,1 at columns 128b + 0.., 2,3 at 128b + 32..)
+          const uint32_t qopt = sb + L::OFF_Q + s * L::STAGE + (SETTING == 1 ? L::QT : 0);
 #pragma unroll
-      for (int kk = 0; kk < KBK / 16; ++kk) {
-        uint32_t a[4];
-        ldsm_x4_t(sw128<KBK>(dsb, kk * 16 + (lane & 7) + (lane >> 4) * 8, 2 * qg + ((lane >> 3) & 1)), a);
+          for (int ks = 0; ks < BQ / 16; ++ks)
+            mma_ts(tmem + kColDK, tmem + 128 * b + (ks >> 1) * 32 + (ks & 1) * 8,
+                   sdesc_sw128(qopt + ks * 2048, BQ * 128, 1024), id_dk, jj > 0 || ks > 0);
+          // dQp^T = K_opt^T dS: A = K_opt (keys x d) read MN-major, B = dS^T (keys x queries) MN-major
+          const uint32_t dsb = sb + L::OFF_DS + b * L::DS_BYTES;
 #pragma unroll
-        for (int np = 0; np < D / 32; ++np) {
-          uint32_t b[4];
-          ldsm_x4_t(sw128<KBK>(kopt, kk * 16 + trow, dh * (D / 16) + 2 * np + tcol), b);
-          mma16816(pq[2 * np], a, b[0], b[1]);
-          mma16816(pq[2 * np + 1], a, b[2], b[3]);
+          for (int ks = 0; ks < BK / 16; ++ks)
+            mma_ss(tmem + kColDQ + 64 * b, sdesc_sw128(kopt + ks * 2048, D == 128 ? BK * 128 : 0, 1024),
+                   sdesc_sw128(dsb + ks * 2048, 0, 1024), id_dq, ks > 0);
+          mma_commit(y_empty + 8 * s);
+          mma_commit(ds_free + 8 * b);
+          mma_commit(dq_full + 8 * b);
         }
       }
+      // all MMAs done (the last dq_full commit covers every earlier MMA)
+      if (n_yt > 0) mbar_drain(dq_full + 8 * ((n_yt - 1) & 1), ((n_yt - 1) >> 1) & 1, status);
+    }
+    __syncwarp();
+  } else if (warp < DS_WARPS) {
+    // ------------------------------------------------------------------ dS warps
+    const int grp = warp >> 2, wq = warp & 3;
+    const int r = wq * 32 + lane;
+    const int key = k0 + r;
+    const float c = p.c;
+    const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
+    for (int j = 0; j < n_yt; ++j) {
+      const int b = j & 1, s = j % STAGES;
+      bool got = mbar_wait(s_full + 8 * b, (j >> 1) & 1, status, abort_flag);
+      __syncwarp();
+      if (!got) break;
+      tc_fence_after();
+      // the per-query values were staged by the producer lanes: acquire them directly
+      got = mbar_wait(y_full + 8 * s, (j / STAGES) & 1, status, abort_flag);
+      __syncwarp();
+      if (!got) break;
+      uint32_t a[32], bb[32];
+      const uint32_t ta = tmem + lane_base + 128 * b + grp * 32;
+      tmem_ld32(ta, a);
+      tmem_ld32(ta + 64, bb);
+      tmem_ld_wait();
+      reg_fence32(a);
+      reg_fence32(bb);
+      const int q0 = q_begin + j * BQ + grp * 32;
+      const float* vals = reinterpret_cast<const float*>(smem + L::OFF_VALS + s * 4 * BQ * 4) + grp * 32;
+      const bool masked = (q0 + 31 >= p.NQ) || (key >= p.NK) || (p.causal && key > q0 + p.off);
+      uint32_t pk[16];
+      if (masked)
+        make_dst<SETTING, true>(a, bb, pk, c, vals, key, q0, p.NQ, p.NK, p.off, p.causal);
+      else
+        make_dst<SETTING, false>(a, bb, pk, c, vals, key, q0, p.NQ, p.NK, p.off, p.causal);
+      // the smem copy of dS^T (B of the dQ MMA) is free once the dQ MMA of tile j-2 is done
+      if (j >= 2) {
+        got = mbar_wait(ds_free + 8 * b, ((j >> 1) - 1) & 1, status, abort_flag);
+        __syncwarp();
+        if (!got) break;
+      }
+      const uint32_t dsb = sb + L::OFF_DS + b * L::DS_BYTES;
 #pragma unroll
-      for (int hr = 0; hr < 2; ++hr) {
-        const int q = q0 + qg * 16 + g + hr * 8;
-        if (q < p.NQ) {
-          float* dst = dq_acc + ((size_t)bh * p.NQ + q) * D + dh * (D / 2) + 2 * t;
+      for (int cch = 0; cch < 4; ++cch) {
+        const uint32_t dst = sw128<BK>(dsb, r, grp * 4 + cch);
+        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(pk[4 * cch]), "r"(pk[4 * cch + 1]),
+                     "r"(pk[4 * cch + 2]), "r"(pk[4 * cch + 3])
+                     : "memory");
+      }
+      fence_async_smem();
+      // packed dS^T over this group's first 16 S1^T columns (already read): A of the dK MMA
+      tmem_st16(tmem + lane_base + 128 * b + grp * 32, pk);
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(s_free + 8 * b);
+        mbar_arrive(ds_full + 8 * b);
+      }
+    }
+    // ---- dK out
+    constexpr int HALF = D / 2;
+    bool got = mbar_wait(dq_full + 8 * ((n_yt - 1) & 1), ((n_yt - 1) >> 1) & 1, status, abort_flag);
+    __syncwarp();
+    if (got) {
+      tc_fence_after();
+      uint32_t g0[32], g1[32];
+      const uint32_t tg = tmem + lane_base + kColDK + grp * HALF;
+      tmem_ld32(tg, g0);
+      if (HALF == 64) tmem_ld32(tg + 32, g1);
+      tmem_ld_wait();
+      reg_fence32(g0);
+      reg_fence32(g1);
+      if (key < p.NK) {
+        __nv_bfloat16* dst = dk_out + ((size_t)bh * p.NK + key) * D + grp * HALF;
 #pragma unroll
-          for (int n = 0; n < D / 16; ++n) red_add_v2(dst + n * 8, pq[n][2 * hr], pq[n][2 * hr + 1]);
+        for (int v = 0; v < HALF / 8; ++v) {
+          uint4 o;
+          const uint32_t* src = v < 4 ? &g0[v * 8] : &g1[(v - 4) * 8];
+          o.x = pack_bf16(__uint_as_float(src[0]) * p.scale, __uint_as_float(src[1]) * p.scale);
+          o.y = pack_bf16(__uint_as_float(src[2]) * p.scale, __uint_as_float(src[3]) * p.scale);
+          o.z = pack_bf16(__uint_as_float(src[4]) * p.scale, __uint_as_float(src[5]) * p.scale);
+          o.w = pack_bf16(__uint_as_float(src[6]) * p.scale, __uint_as_float(src[7]) * p.scale);
+          reinterpret_cast<uint4*>(dst)[v] = o;
         }
       }
     }
-  }
-  if (!ok) return;
+  } else {
+    // ------------------------------------------------------------------ dQ warps
+    const int wq = warp - DQ_WARP0;
+    const int d = wq * 32 + lane;  // lane of dQp^T = column d
+    const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
+    for (int j = 0; j < n_yt; ++j) {
+      const int b = j & 1;
+      const bool got = mbar_wait(dq_full + 8 * b, (j >> 1) & 1, status, abort_flag);
+      __syncwarp();
+      if (!got) break;
+      tc_fence_after();
+      uint32_t v0[32], v1[32];
+      tmem_ld32(tmem + lane_base + kColDQ + 64 * b, v0);
+      tmem_ld32(tmem + lane_base + kColDQ + 64 * b + 32, v1);
+      tmem_ld_wait();
+      reg_fence32(v0);
+      reg_fence32(v1);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(dq_free + 8 * b);
+      if (d < D) {
+        const int q0 = q_begin + j * BQ;
+        float* base = dq_acc + ((size_t)bh * p.NQ + q0) * D + d;
+        const int nrow = min(BQ, p.NQ - q0);
 #pragma unroll
-  for (int hr = 0; hr < 2; ++hr) {
-    const int key = key0 + hr * 8;
-    if (key < p.NK) {
-      __nv_bfloat16* dst = dk_out + ((size_t)bh * p.NK + key) * D + 2 * t;
+        for (int i = 0; i < 32; ++i)
+          if (i < nrow) red_add_f32(base + (size_t)i * D, __uint_as_float(v0[i]));
 #pragma unroll
-      for (int n = 0; n < D / 8; ++n)
-        *reinterpret_cast<uint32_t*>(dst + n * 8) =
-            pack_bf16(dk[n][2 * hr] * p.scale, dk[n][2 * hr + 1] * p.scale);
+        for (int i = 0; i < 32; ++i)
+          if (32 + i < nrow) red_add_f32(base + (size_t)(32 + i) * D, __uint_as_float(v1[i]));
+      }
     }
   }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == MMA_WARP) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+constexpr int kOneBlockPerSmSmem = 120 * 1024;  // a block owns all 512 TMEM columns
+
+template <int D, int SETTING>
+cudaError_t launch_fused(const Problem& p, const BwdIn& in, void* dk, float* dq_acc, int* status, cudaStream_t st) {
+  CUtensorMap mk1, mk2, mq1, mq2;
+  if (!encode_tile_map(&mk1, in.k1, D, p.NK, p.BH, BK) || !encode_tile_map(&mk2, in.k2, D, p.NK, p.BH, BK) ||
+      !encode_tile_map(&mq1, in.q1, D, p.NQ, p.BH, BQ) || !encode_tile_map(&mq2, in.q2, D, p.NQ, p.BH, BQ))
+    return cudaErrorInvalidValue;
+  const int smem = Smem<D>::BYTES > kOneBlockPerSmSmem ? Smem<D>::BYTES : kOneBlockPerSmSmem;
+  auto kern = bwd_fused_tc_kernel<D, SETTING>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  const long long blocks = (long long)p.BH * ((p.NK + BK - 1) / BK);
+  kern<<<(unsigned)blocks, THREADS, smem, st>>>(p, in.lse1, in.lse2, in.kl, in.g, static_cast<__nv_bfloat16*>(dk),
+                                                dq_acc, status, mk1, mk2, mq1, mq2);
+  return cudaGetLastError();
 }
 
 // dQ (bf16) = scale * dQ accumulator (fp32); 8 elements per thread.
@@ -295,31 +409,14 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const float4* __restric
   }
 }
 
-// FUSED = false is the separate-path dK form of the same loop; only the fused
-// form is launched (the separate path runs on tcgen05, bwd_tc.cu).
-template <int D, int SETTING, bool FUSED>
-cudaError_t launch_dk(const Problem& p, const BwdIn& in, void* dk, float* dq_acc, int* status, cudaStream_t st) {
-  CUtensorMap mq1, mk1, mq2, mk2;
-  if (!encode_tile_map(&mq1, in.q1, D, p.NQ, p.BH, KBQ) || !encode_tile_map(&mq2, in.q2, D, p.NQ, p.BH, KBQ) ||
-      !encode_tile_map(&mk1, in.k1, D, p.NK, p.BH, KBK) || !encode_tile_map(&mk2, in.k2, D, p.NK, p.BH, KBK))
-    return cudaErrorInvalidValue;
-  const int smem = DkSmem<D, FUSED>::BYTES;
-  auto kern = bwd_dk_kernel<D, SETTING, FUSED>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
-  kern<<<dim3(p.BH, (p.NK + KBK - 1) / KBK), THREADS, smem, st>>>(
-      p, in.lse1, in.lse2, in.kl, in.g, static_cast<__nv_bfloat16*>(dk), dq_acc, status, mq1, mk1, mq2, mk2);
-  return cudaGetLastError();
-}
-
 template <int D>
 cudaError_t fused_d(const Problem& p, int setting, const BwdIn& in, void* dq, void* dk, float* dq_acc, int* status,
                     cudaStream_t st) {
   const size_t n = (size_t)p.BH * p.NQ * D;
   cudaError_t e = cudaMemsetAsync(dq_acc, 0, n * sizeof(float), st);
   if (e != cudaSuccess) return e;
-  e = setting == 1 ? launch_dk<D, 1, true>(p, in, dk, dq_acc, status, st)
-                   : launch_dk<D, 2, true>(p, in, dk, dq_acc, status, st);
+  e = setting == 1 ? launch_fused<D, 1>(p, in, dk, dq_acc, status, st)
+                   : launch_fused<D, 2>(p, in, dk, dq_acc, status, st);
   if (e != cudaSuccess) return e;
   const size_t n8 = n / 8;
   const int blocks = (int)((n8 + 255) / 256 < 4096 ? (n8 + 255) / 256 : 4096);

@@ -266,7 +266,8 @@ def run_ours(args):
     decode = w.name.startswith("decode")
     mode = {"auto": skl.BWD_AUTO, "fused": skl.BWD_FUSED, "separate": skl.BWD_SEPARATE}[args.bwd_mode]
     if not decode and mode == skl.BWD_AUTO:
-        mode = skl.bwd_select(w.B, w.H, w.NQ, w.NK, w.D, torch.cuda.get_device_properties(dev).L2_cache_size,
+        props = torch.cuda.get_device_properties(dev)
+        mode = skl.bwd_select(w.B, w.H, w.NQ, w.NK, w.D, props.L2_cache_size, props.multi_processor_count,
                               w.causal)
     inp = synth.make_inputs(w)
     host = [torch.from_numpy(inp[k].view(np.int16)).view(torch.bfloat16) for k in ("q1", "k1", "q2", "k2")]

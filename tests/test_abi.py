@@ -149,13 +149,25 @@ def test_splitk_plan_minimises_the_wave_model(lib, bh, nk, sms):
         assert ideal / _cost(bh, tiles, sms, s) > 0.9
 
 
+def _live_rows_bytes(B, H, NQ, NK, D, sms):
+    key_tiles = -(-NK // 128)
+    heads = min(B * H, -(-sms // key_tiles) + 1)
+    return NQ * D * 4 * heads
+
+
 def test_bwd_select_rule(lib):
-    # fused exactly while the fp32 dQ buffer [B,H,N_Q,D] fits in L2
-    l2 = 126 * 2**20
-    assert K.bwd_select(1, 1, 128, 128, 64, l2) == K.BWD_FUSED
-    fits = 126 * 2**20 // (32 * 128 * 4)
-    assert K.bwd_select(1, 32, fits, fits, 128, l2) == K.BWD_FUSED
-    assert K.bwd_select(1, 32, fits + 1, fits + 1, 128, l2) == K.BWD_SEPARATE
-    assert K.bwd_select(2, 32, 4096, 4096, 128, l2) == K.BWD_SEPARATE  # 128 MiB > 126 MiB
-    assert K.bwd_select(1, 32, 65536, 65536, 128, l2) == K.BWD_SEPARATE
-    assert K.bwd_select(0, 1, 8, 8, 64, l2) == 0  # invalid shape
+    # fused exactly while the live dQ rows (heads in flight x N_Q x D x 4 B) fit in L2
+    l2, sms = 135528448, 152  # GB300
+    assert K.bwd_select(1, 1, 128, 128, 64, l2, sms) == K.BWD_FUSED
+    assert K.bwd_select(2, 32, 4096, 4096, 128, l2, sms) == K.BWD_FUSED  # whole buffer 128 MiB; live 12 MiB
+    assert K.bwd_select(1, 32, 65536, 65536, 128, l2, sms) == K.BWD_FUSED  # live: 2 heads x 32 MiB
+    assert K.bwd_select(1, 8, 524288, 524288, 128, l2, sms) == K.BWD_SEPARATE  # one head's rows: 256 MiB
+    for n in (100000, 120000, 131072, 140000, 200000):
+        want = K.BWD_FUSED if _live_rows_bytes(1, 8, n, n, 128, sms) <= l2 else K.BWD_SEPARATE
+        assert K.bwd_select(1, 8, n, n, 128, l2, sms) == want, n
+    # few key tiles: a wave spans many heads, all of whose rows are live
+    assert _live_rows_bytes(64, 32, 4096, 256, 128, sms) == 4096 * 128 * 4 * 77
+    assert K.bwd_select(64, 32, 4096, 256, 128, 77 * 4096 * 512, sms) == K.BWD_FUSED
+    assert K.bwd_select(64, 32, 4096, 256, 128, 77 * 4096 * 512 - 1, sms) == K.BWD_SEPARATE
+    assert K.bwd_select(0, 1, 8, 8, 64, l2, sms) == 0  # invalid shape
+    assert K.bwd_select(1, 1, 8, 8, 64, l2, 0) == 0  # no SM count

@@ -180,7 +180,8 @@ def test_b1h8_n524288_causal_setting2():
     w = W["kl_b1h8_n524288_d128_causal"]
     inp = synth.make_inputs(w)
     kl, l1, l2 = _run_fwd(inp, w)
-    assert skl.bwd_select(w.B, w.H, w.NQ, w.NK, w.D, torch.cuda.get_device_properties(0).L2_cache_size,
+    props = torch.cuda.get_device_properties(0)
+    assert skl.bwd_select(w.B, w.H, w.NQ, w.NK, w.D, props.L2_cache_size, props.multi_processor_count,
                           w.causal) == skl.BWD_SEPARATE
     dq, dk = _run_bwd(inp, w, 2, skl.BWD_AUTO, kl, l1, l2)
     torch.cuda.synchronize()
