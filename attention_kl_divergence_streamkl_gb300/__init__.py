@@ -8,3 +8,4 @@ from ._lib import (BWD_AUTO, BWD_DK_ONLY, BWD_DQ_ONLY, BWD_FUSED, BWD_SEPARATE, 
                    Shape, StreamKLError,
                    bwd_s1, bwd_s2, bwd_select, bwd_workspace_bytes, check_device_status, debug_wait_timeout,
                    fwd, fwd_splitk, lib, make_shape, splitk_plan, status_string)
+from .autograd import attention_kl  # noqa: E402,F401

@@ -54,47 +54,56 @@ struct Smem {
   static constexpr int BYTES = OFF_BAR + 8 * 19 + 16 + 1024;
 };
 
+// Per-query values staged for a tile, three arrays of BQ floats, folded so the
+// element loop needs one packed FMA per logit:
+//   nA = -LSE1 log2(e)
+//   nB = -LSE2 log2(e)                    (setting 1)
+//        -(LSE1 - LSE2 + KL)              (setting 2; the log ratio minus KL is then
+//                                          scale (S1 - S2) + nB, from logits and LSEs)
+//   G  = g
 template <int SETTING, bool MASKED>
 __device__ __forceinline__ void make_dst(const uint32_t (&a)[32], const uint32_t (&b)[32], uint32_t (&pk)[16],
-                                         float c, const float* vals, int key, int q0, int nq, int nk, int off,
-                                         int causal) {
+                                         float c, float scale, const float* vals, int key, int q0, int nq, int nk,
+                                         int off, int causal) {
   // thread = one key; 32 query columns q0 .. q0 + 31 with their values in vals[*][0..31]
+  const float2 cc = make_float2(c, c), sc = make_float2(scale, scale);
 #pragma unroll
-  for (int i = 0; i < 32; i += 2) {
-    const float2 s1 = make_float2(__uint_as_float(a[i]), __uint_as_float(a[i + 1]));
-    const float2 s2 = make_float2(__uint_as_float(b[i]), __uint_as_float(b[i + 1]));
-    const float2 L1 = make_float2(vals[i], vals[i + 1]);
-    const float2 L2 = make_float2(vals[BQ + i], vals[BQ + i + 1]);
-    const float2 G = make_float2(vals[2 * BQ + i], vals[2 * BQ + i + 1]);
-    const float2 cc = make_float2(c, c);
-    const float2 x1 = ffma2(s1, cc, make_float2(-L1.x, -L1.y));
-    float2 p1 = make_float2(ex2(x1.x), ex2(x1.y));
-    float2 ds;
-    if (SETTING == 1) {
-      const float2 x2 = ffma2(s2, cc, make_float2(-L2.x, -L2.y));
-      float2 p2 = make_float2(ex2(x2.x), ex2(x2.y));
+  for (int i = 0; i < 32; i += 4) {
+    const float4 nA4 = *reinterpret_cast<const float4*>(vals + i);
+    const float4 nB4 = *reinterpret_cast<const float4*>(vals + BQ + i);
+    const float4 G4 = *reinterpret_cast<const float4*>(vals + 2 * BQ + i);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int k = i + 2 * h;
+      const float2 nA = h ? make_float2(nA4.z, nA4.w) : make_float2(nA4.x, nA4.y);
+      const float2 nB = h ? make_float2(nB4.z, nB4.w) : make_float2(nB4.x, nB4.y);
+      const float2 G = h ? make_float2(G4.z, G4.w) : make_float2(G4.x, G4.y);
+      const float2 s1 = make_float2(__uint_as_float(a[k]), __uint_as_float(a[k + 1]));
+      const float2 s2 = make_float2(__uint_as_float(b[k]), __uint_as_float(b[k + 1]));
+      const float2 x1 = ffma2(s1, cc, nA);
+      float2 p1 = make_float2(ex2(x1.x), ex2(x1.y));
+      bool k0 = true, k1 = true;
       if (MASKED) {
-        const int q = q0 + i;
-        const bool k0 = q < nq && key < nk && (!causal || key <= q + off);
-        const bool k1 = q + 1 < nq && key < nk && (!causal || key <= q + 1 + off);
+        const int q = q0 + k;
+        k0 = q < nq && key < nk && (!causal || key <= q + off);
+        k1 = q + 1 < nq && key < nk && (!causal || key <= q + 1 + off);
         p1.x = k0 ? p1.x : 0.f;
         p1.y = k1 ? p1.y : 0.f;
-        p2.x = k0 ? p2.x : 0.f;
-        p2.y = k1 ? p2.y : 0.f;
       }
-      ds = fmul2(G, fsub2(p2, p1));
-    } else {
-      if (MASKED) {
-        const int q = q0 + i;
-        p1.x = (q < nq && key < nk && (!causal || key <= q + off)) ? p1.x : 0.f;
-        p1.y = (q + 1 < nq && key < nk && (!causal || key <= q + 1 + off)) ? p1.y : 0.f;
+      float2 ds;
+      if (SETTING == 1) {
+        const float2 x2 = ffma2(s2, cc, nB);
+        float2 p2 = make_float2(ex2(x2.x), ex2(x2.y));
+        if (MASKED) {
+          p2.x = k0 ? p2.x : 0.f;
+          p2.y = k1 ? p2.y : 0.f;
+        }
+        ds = fmul2(G, fsub2(p2, p1));
+      } else {
+        ds = fmul2(fmul2(G, p1), ffma2(sc, fsub2(s1, s2), nB));
       }
-      const float2 KL = make_float2(vals[3 * BQ + i], vals[3 * BQ + i + 1]);
-      // r = ln2 ((s1 - s2) c - (L1 - L2))
-      const float2 r = fmul2(make_float2(kLn2, kLn2), ffma2(fsub2(s1, s2), cc, fsub2(L2, L1)));
-      ds = fmul2(fmul2(G, p1), fsub2(r, KL));
+      pk[k / 2] = pack_bf16(ds.x, ds.y);
     }
-    pk[i / 2] = pack_bf16(ds.x, ds.y);
   }
 }
 
@@ -181,10 +190,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int qi = lane + 32 * k, q = q0 + qi;
         const bool in = q < p.NQ;
         const size_t o = (size_t)bh * p.NQ + q;
-        vals[qi] = in ? lse1[o] * kLog2e : 0.f;
-        vals[BQ + qi] = in ? lse2[o] * kLog2e : 0.f;
+        const float l1v = in ? lse1[o] : 0.f, l2v = in ? lse2[o] : 0.f;
+        vals[qi] = -l1v * kLog2e;
+        vals[BQ + qi] = SETTING == 1 ? -l2v * kLog2e : -(l1v - l2v + (in ? klv[o] : 0.f));
         vals[2 * BQ + qi] = in ? gv[o] : 0.f;
-        vals[3 * BQ + qi] = (SETTING == 2 && in) ? klv[o] : 0.f;
       }
       mbar_arrive(y_full + 8 * s);
       issued = j + 1;
@@ -202,6 +211,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       constexpr uint32_t id_dk = idesc_bf16(BK, D, false, true);
       constexpr uint32_t id_dq = idesc_bf16(128, BQ, true, true);
       const uint32_t kopt = sb + (SETTING == 1 ? L::OFF_K2 : L::OFF_K1);
+      const uint64_t k1d = sdesc_sw128(sb + L::OFF_K1, 0, 1024), k2d = sdesc_sw128(sb + L::OFF_K2, 0, 1024);
+      const uint64_t kod = sdesc_sw128(kopt, D == 128 ? BK * 128 : 0, 1024);
       bool ok = mbar_wait(k_full, 0, status, abort_flag);
       for (int j = 0; ok && j <= n_yt; ++j) {
         if (j < n_yt) {
@@ -210,19 +221,18 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (j >= 2 && !mbar_wait(s_free + 8 * b, ((j >> 1) - 1) & 1, status, abort_flag)) break;
           tc_fence_after();
           const uint32_t q1 = sb + L::OFF_Q + s * L::STAGE, q2 = q1 + L::QT;
+          const uint64_t q1d = sdesc_sw128(q1, 0, 1024), q2d = sdesc_sw128(q2, 0, 1024);
 #pragma unroll
           for (int ks = 0; ks < D / 16; ++ks) {
             const uint32_t ka = (ks >> 2) * (BK * 128) + (ks & 3) * 32;  // 128-key tile halves
             const uint32_t qa = (ks >> 2) * (BQ * 128) + (ks & 3) * 32;  // 64-query tile halves
-            mma_ss(tmem + 128 * b, sdesc_sw128(sb + L::OFF_K1 + ka, 0, 1024), sdesc_sw128(q1 + qa, 0, 1024), id_s,
-                   ks > 0);
+            mma_ss(tmem + 128 * b, sdesc_add(k1d, ka), sdesc_add(q1d, qa), id_s, ks > 0);
           }
 #pragma unroll
           for (int ks = 0; ks < D / 16; ++ks) {
             const uint32_t ka = (ks >> 2) * (BK * 128) + (ks & 3) * 32;
             const uint32_t qa = (ks >> 2) * (BQ * 128) + (ks & 3) * 32;
-            mma_ss(tmem + 128 * b + 64, sdesc_sw128(sb + L::OFF_K2 + ka, 0, 1024), sdesc_sw128(q2 + qa, 0, 1024),
-                   id_s, ks > 0);
+            mma_ss(tmem + 128 * b + 64, sdesc_add(k2d, ka), sdesc_add(q2d, qa), id_s, ks > 0);
           }
           mma_commit(s_full + 8 * b);
         }
@@ -232,17 +242,16 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (jj >= 2 && !mbar_wait(dq_free + 8 * b, ((jj >> 1) - 1) & 1, status, abort_flag)) break;
           tc_fence_after();
           // dK += dS^T Q_opt: A = packed dS^T in TMEM (query k-steps 0,1 at columns 128b + 0.., 2,3 at 128b + 32..)
-          const uint32_t qopt = sb + L::OFF_Q + s * L::STAGE + (SETTING == 1 ? L::QT : 0);
+          const uint64_t qod = sdesc_sw128(sb + L::OFF_Q + s * L::STAGE + (SETTING == 1 ? L::QT : 0), BQ * 128, 1024);
 #pragma unroll
           for (int ks = 0; ks < BQ / 16; ++ks)
-            mma_ts(tmem + kColDK, tmem + 128 * b + (ks >> 1) * 32 + (ks & 1) * 8,
-                   sdesc_sw128(qopt + ks * 2048, BQ * 128, 1024), id_dk, jj > 0 || ks > 0);
+            mma_ts(tmem + kColDK, tmem + 128 * b + (ks >> 1) * 32 + (ks & 1) * 8, sdesc_add(qod, ks * 2048), id_dk,
+                   jj > 0 || ks > 0);
           // dQp^T = K_opt^T dS: A = K_opt (keys x d) read MN-major, B = dS^T (keys x queries) MN-major
-          const uint32_t dsb = sb + L::OFF_DS + b * L::DS_BYTES;
+          const uint64_t dsd = sdesc_sw128(sb + L::OFF_DS + b * L::DS_BYTES, 0, 1024);
 #pragma unroll
           for (int ks = 0; ks < BK / 16; ++ks)
-            mma_ss(tmem + kColDQ + 64 * b, sdesc_sw128(kopt + ks * 2048, D == 128 ? BK * 128 : 0, 1024),
-                   sdesc_sw128(dsb + ks * 2048, 0, 1024), id_dq, ks > 0);
+            mma_ss(tmem + kColDQ + 64 * b, sdesc_add(kod, ks * 2048), sdesc_add(dsd, ks * 2048), id_dq, ks > 0);
           mma_commit(y_empty + 8 * s);
           mma_commit(ds_free + 8 * b);
           mma_commit(dq_full + 8 * b);
@@ -281,9 +290,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       const bool masked = (q0 + 31 >= p.NQ) || (key >= p.NK) || (p.causal && key > q0 + p.off);
       uint32_t pk[16];
       if (masked)
-        make_dst<SETTING, true>(a, bb, pk, c, vals, key, q0, p.NQ, p.NK, p.off, p.causal);
+        make_dst<SETTING, true>(a, bb, pk, c, p.scale, vals, key, q0, p.NQ, p.NK, p.off, p.causal);
       else
-        make_dst<SETTING, false>(a, bb, pk, c, vals, key, q0, p.NQ, p.NK, p.off, p.causal);
+        make_dst<SETTING, false>(a, bb, pk, c, p.scale, vals, key, q0, p.NQ, p.NK, p.off, p.causal);
       // the smem copy of dS^T (B of the dQ MMA) is free once the dQ MMA of tile j-2 is done
       if (j >= 2) {
         got = mbar_wait(ds_free + 8 * b, ((j >> 1) - 1) & 1, status, abort_flag);

@@ -206,6 +206,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   } else if (warp == MMA_WARP) {
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_bf16(BM, BN, false, false);
+      const uint64_t q1d = sdesc_sw128(sb + L::OFF_Q1, 0, 1024), q2d = sdesc_sw128(sb + L::OFF_Q2, 0, 1024);
       int issued = 0;
       bool ok = mbar_wait(bar_q, 0, status, abort_flag);
       for (int j = 0; ok && j < n_kt; ++j) {
@@ -215,15 +216,16 @@ __global__ void __launch_bounds__(THREADS, 1)
         tc_fence_after();
         const uint32_t kb1 = sb + L::OFF_K + s * L::STAGE, kb2 = kb1 + L::K_BYTES;
         const uint32_t d1 = tmem + s * 256, d2 = d1 + 128;
+        const uint64_t k1d = sdesc_sw128(kb1, 0, 1024), k2d = sdesc_sw128(kb2, 0, 1024);
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
           const uint32_t off = (ks >> 2) * (BM * 128) + (ks & 3) * 32;  // BM == BN: same half stride
-          mma_ss(d1, sdesc_sw128(sb + L::OFF_Q1 + off, 0, 1024), sdesc_sw128(kb1 + off, 0, 1024), idesc, ks > 0);
+          mma_ss(d1, sdesc_add(q1d, off), sdesc_add(k1d, off), idesc, ks > 0);
         }
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
           const uint32_t off = (ks >> 2) * (BM * 128) + (ks & 3) * 32;
-          mma_ss(d2, sdesc_sw128(sb + L::OFF_Q2 + off, 0, 1024), sdesc_sw128(kb2 + off, 0, 1024), idesc, ks > 0);
+          mma_ss(d2, sdesc_add(q2d, off), sdesc_add(k2d, off), idesc, ks > 0);
         }
         mma_commit(bar_sfull + 8 * s);
         mma_commit(bar_empty + 8 * s);

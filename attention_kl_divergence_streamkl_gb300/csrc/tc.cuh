@@ -33,6 +33,11 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_byt
          ((uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
 }
 
+// The descriptor of shared address a + off is the descriptor of a plus off >> 4:
+// the start-address field holds a >> 4, below 2^14 for any shared-memory
+// address, so inner loops add constants to a descriptor computed once.
+__device__ __forceinline__ uint64_t sdesc_add(uint64_t desc, uint32_t byte_off) { return desc + (byte_off >> 4); }
+
 // ---- TMEM allocation (whole warp)
 __device__ __forceinline__ void tmem_alloc(uint32_t slot_saddr, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot_saddr), "r"(ncols)
