@@ -8,18 +8,27 @@
 // bwd_tc.cu (setting 1: dS2 = g (P2 - P1); setting 2: dS1 = g P1 (r - KL)).
 //
 // Block = one 128-key tile (stationary K1, K2 in smem; keys on the 128 TMEM
-// lanes), streaming 64-query tiles Y:
-//   S1^T = K1 Q1^T, S2^T = K2 Q2^T    SS, M = 128 keys, N = 64 queries (double-buffered in TMEM)
-//   dS^T from S^T and the per-query LSE1, LSE2, g, KL of the tile
-//   dK  += dS^T Q_opt                 TS: A = dS^T packed bf16 over S1^T's columns, B = Q_opt MN-major
-//   dQp^T = K_opt^T dS                SS: A = K_opt read MN-major (M = D on lanes), B = dS^T in smem
+// lanes), streaming 128-query tiles Y.  Every MMA is M = 128, N = 128: on this
+// GPU a single-CTA M = 128 MMA costs the same for any N up to 128, so narrower
+// tiles only waste the tensor core.
+//   S1^T = K1 Q1^T, S2^T = K2 Q2^T    SS, K-major, into TMEM columns [0, 128) and [128, 256)
+//   dS^T from S^T and the per-query LSE1, LSE2, g, KL of the tile, written to smem as dS[key][query]
+//   dK  += dS^T Q_opt                 SS: A = dS (K-major over queries), B = Q_opt MN-major  -> [256, 256 + D)
+//   dQp^T = K_opt^T dS                SS: A = K_opt read MN-major (M = d), B = dS MN-major   -> [384, 512)
 //   dq_acc[q, d] += dQp^T[d, q]       one warp adds 32 consecutive d of one query row (128 B) per red
-// TMEM: S^T buffer b at [128b, 128b + 128) (S1^T then S2^T, 64 columns each),
-// dK at [256, 256 + D), dQp^T buffer b at [384 + 64b, 448 + 64b).
-//   warp 12     TMA producer; its 32 lanes also stage the per-query values
-//   warp 13     TMEM owner and MMA issuer (S(j) issued before dK/dQp of tile j-1)
-//   warps 0-7   dS warps: thread = key row, group g = query columns [32g, 32g + 32)
-//   warps 8-11  dQ warps: thread = column d of dQp^T, reduce-add into dq_acc
+// TMEM holds one S tile, so the dS warps copy their part of S^T into registers
+// first and release it: S of the next tile is computed while they work.  The
+// same warps drain the previous tile's dQp^T (a 32 x 32 block each) before they
+// publish dS, so one barrier tells the MMA issuer that both dS and the dQp^T
+// columns are ready.
+//   warps 0-15  dS warps: thread = key row (lane quarter = warp % 4), group g = warp / 4
+//               takes query columns [32g, 32g + 32); for dQp^T, thread = column d
+//   warp 16     TMA producer (K1, K2 once; Q1, Q2 through two stages)
+//   warp 17     TMEM owner and MMA issuer (S(j) issued before dK/dQp of tile j-1)
+//   warp 18     stages the per-query values of each tile in smem
+// Warpgroup 4 gives registers to the dS warpgroups (setmaxnreg).
+#include <utility>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "tc.cuh"
@@ -28,31 +37,56 @@ namespace skl {
 namespace {
 
 constexpr int BK = 128;  // keys per block (M of the S and dK MMAs)
-constexpr int BQ = 64;   // queries per step
-constexpr int STAGES = 3;
-constexpr int DS_WARPS = 8;
-constexpr int DQ_WARP0 = 8;
-constexpr int PRODUCER_WARP = 12;
-constexpr int MMA_WARP = 13;
-constexpr int THREADS = 14 * 32;
+constexpr int BQ = 128;  // queries per step (N of the S and dQp MMAs)
+constexpr int STAGES = 2;
+constexpr int DS_WARPS = 16;
+constexpr int PRODUCER_WARP = 16;
+constexpr int MMA_WARP = 17;
+constexpr int VALS_WARP = 18;
+constexpr int THREADS = 20 * 32;
+constexpr int kRegsDs = 104, kRegsOther = 64;  // 512 * 104 + 128 * 64 = 640 * 96 registers at launch
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColDK = 256, kColDQ = 384;
+constexpr uint32_t kColS1 = 0, kColS2 = 128, kColDK = 256, kColDQ = 384;
 
 template <int D>
 struct Smem {
-  static constexpr int KT = BK * D * 2;   // one 128-key tile
-  static constexpr int QT = BQ * D * 2;   // one 64-query tile (D/64 halves of 8 KiB)
+  static constexpr int KT = BK * D * 2;  // one 128-key tile (D/64 halves of [128][128 B])
+  static constexpr int QT = BQ * D * 2;  // one 128-query tile
   static constexpr int OFF_K1 = 0;
   static constexpr int OFF_K2 = KT;
   static constexpr int OFF_Q = 2 * KT;  // stage s: Q1, Q2
   static constexpr int STAGE = 2 * QT;
-  static constexpr int OFF_DS = OFF_Q + STAGES * STAGE;  // [2][128 keys][64 queries] bf16, 16 KiB each
+  static constexpr int OFF_DS = OFF_Q + STAGES * STAGE;  // dS[key][query] bf16: 2 halves of [128 keys][128 B]
   static constexpr int DS_BYTES = BK * BQ * 2;
-  static constexpr int OFF_VALS = OFF_DS + 2 * DS_BYTES;  // [STAGES][4][64] fp32
-  static constexpr int OFF_BAR = OFF_VALS + STAGES * 4 * BQ * 4;
-  // k_full, y_full[3], y_empty[3], s_full[2], s_free[2], ds_full[2], ds_free[2], dq_full[2], dq_free[2], slot, abort
-  static constexpr int BYTES = OFF_BAR + 8 * 19 + 16 + 1024;
+  static constexpr int OFF_VALS = OFF_DS + DS_BYTES;  // [3][BQ] fp32, one tile
+  static constexpr int OFF_BAR = OFF_VALS + 3 * BQ * 4;
+  // mbarriers (8 B each): k_full, y_full[STAGES], y_empty[STAGES], s_full, s_free, v_full, v_free,
+  // ds_full, ds_free, all_done; then the TMEM base address slot and the abort flag
+  static constexpr int BAR_Y_FULL = 8, BAR_Y_EMPTY = BAR_Y_FULL + 8 * STAGES, BAR_ONE = BAR_Y_EMPTY + 8 * STAGES;
+  static constexpr int BAR_SLOT = BAR_ONE + 7 * 8;
+  static constexpr int BYTES = OFF_BAR + BAR_SLOT + 16 + 1024;
 };
+static_assert(Smem<128>::BYTES <= 227 * 1024, "shared memory");
+
+__device__ __forceinline__ void setmaxnreg_inc_ds() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsDs));
+}
+__device__ __forceinline__ void setmaxnreg_dec_other() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsOther));
+}
+
+// red.global.add.f32 at base + OFF bytes: the offset rides in the instruction,
+// so a row loop keeps one 64-bit address live instead of one per row.
+template <int OFF>
+__device__ __forceinline__ void red_add_at(float* base, float a) {
+  asm volatile("red.global.add.f32 [%0+%2], %1;" ::"l"(base), "f"(a), "n"(OFF) : "memory");
+}
+// base[i * D] += v[i] for the rows i < nrow of a 32-row block
+template <int D, int... I>
+__device__ __forceinline__ void red_rows(float* base, const uint32_t (&v)[32], int nrow,
+                                         std::integer_sequence<int, I...>) {
+  ((I < nrow ? red_add_at<I * D * 4>(base, __uint_as_float(v[I])) : void()), ...);
+}
 
 // Per-query values staged for a tile, three arrays of BQ floats, folded so the
 // element loop needs one packed FMA per logit:
@@ -61,14 +95,24 @@ struct Smem {
 //        -(LSE1 - LSE2 + KL)              (setting 2; the log ratio minus KL is then
 //                                          scale (S1 - S2) + nB, from logits and LSEs)
 //   G  = g
-template <int SETTING, bool MASKED>
-__device__ __forceinline__ void make_dst(const uint32_t (&a)[32], const uint32_t (&b)[32], uint32_t (&pk)[16],
-                                         float c, float scale, const float* vals, int key, int q0, int nq, int nk,
-                                         int off, int causal) {
-  // thread = one key; 32 query columns q0 .. q0 + 31 with their values in vals[*][0..31]
+// Bit k set iff query column q0 + k (k < N <= 16) sees `key`: the key exists,
+// the query exists, and (causal) key <= query + off.
+template <int N>
+__device__ __forceinline__ uint32_t visible_cols(int key, int q0, int nq, int nk, int off, int causal) {
+  if (key >= nk) return 0u;
+  const int lo = causal ? min(max(key - off - q0, 0), N) : 0;
+  const int hi = min(max(nq - q0, 0), N);
+  return hi > lo ? ((1u << hi) - 1u) & ~((1u << lo) - 1u) : 0u;
+}
+
+template <int SETTING, bool MASKED, int N>
+__device__ __forceinline__ void make_dst(const uint32_t (&a)[N], const uint32_t (&b)[N], uint32_t* pk, float c,
+                                         float scale, const float* vals, uint32_t visible) {
+  // thread = one key; N query columns with their values in vals[*][0..N-1]; with
+  // MASKED, column k contributes only if bit k of `visible` is set
   const float2 cc = make_float2(c, c), sc = make_float2(scale, scale);
 #pragma unroll
-  for (int i = 0; i < 32; i += 4) {
+  for (int i = 0; i < N; i += 4) {
     const float4 nA4 = *reinterpret_cast<const float4*>(vals + i);
     const float4 nB4 = *reinterpret_cast<const float4*>(vals + BQ + i);
     const float4 G4 = *reinterpret_cast<const float4*>(vals + 2 * BQ + i);
@@ -84,9 +128,8 @@ __device__ __forceinline__ void make_dst(const uint32_t (&a)[32], const uint32_t
       float2 p1 = make_float2(ex2(x1.x), ex2(x1.y));
       bool k0 = true, k1 = true;
       if (MASKED) {
-        const int q = q0 + k;
-        k0 = q < nq && key < nk && (!causal || key <= q + off);
-        k1 = q + 1 < nq && key < nk && (!causal || key <= q + 1 + off);
+        k0 = (visible >> k) & 1u;
+        k1 = (visible >> (k + 1)) & 1u;
         p1.x = k0 ? p1.x : 0.f;
         p1.y = k1 ? p1.y : 0.f;
       }
@@ -127,25 +170,25 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int n_yt = (p.NQ - q_begin + BQ - 1) / BQ;
 
   const uint32_t bar = sb + L::OFF_BAR;
-  const uint32_t k_full = bar, y_full = bar + 8, y_empty = bar + 32, s_full = bar + 56, s_free = bar + 72,
-                 ds_full = bar + 88, ds_free = bar + 104, dq_full = bar + 120, dq_free = bar + 136,
-                 slot = bar + 152;
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_BAR + 156);
+  const uint32_t k_full = bar, y_full = bar + L::BAR_Y_FULL, y_empty = bar + L::BAR_Y_EMPTY,
+                 s_full = bar + L::BAR_ONE, s_free = s_full + 8, v_full = s_full + 16, v_free = s_full + 24,
+                 ds_full = s_full + 32, ds_free = s_full + 40, all_done = s_full + 48, slot = bar + L::BAR_SLOT;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_BAR + L::BAR_SLOT + 4);
+  float* vals = reinterpret_cast<float*>(smem + L::OFF_VALS);
 
   if (threadIdx.x == 0) {
     mbar_init(k_full, 1);
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(y_full + 8 * s, 32);
+      mbar_init(y_full + 8 * s, 1);
       mbar_init(y_empty + 8 * s, 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(s_full + 8 * b, 1);
-      mbar_init(s_free + 8 * b, DS_WARPS);
-      mbar_init(ds_full + 8 * b, DS_WARPS);
-      mbar_init(ds_free + 8 * b, 1);
-      mbar_init(dq_full + 8 * b, 1);
-      mbar_init(dq_free + 8 * b, 4);
-    }
+    mbar_init(s_full, 1);
+    mbar_init(s_free, DS_WARPS);
+    mbar_init(v_full, 1);
+    mbar_init(v_free, DS_WARPS);
+    mbar_init(ds_full, DS_WARPS);
+    mbar_init(ds_free, 1);
+    mbar_init(all_done, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -156,150 +199,202 @@ __global__ void __launch_bounds__(THREADS, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::OFF_BAR + 152);
-
-  if (warp == PRODUCER_WARP) {
-    // ------------------------------------------------------------------ producer
-    if (lane == 0) {
-      mbar_arrive_expect_tx(k_full, 2 * L::KT);
-#pragma unroll
-      for (int h = 0; h < D / 64; ++h) {
-        tma_load_3d(sb + L::OFF_K1 + h * BK * 128, &mk1, k_full, h * 64, k0, bh);
-        tma_load_3d(sb + L::OFF_K2 + h * BK * 128, &mk2, k_full, h * 64, k0, bh);
-      }
-    }
-    int issued = 0;
-    for (int j = 0; j < n_yt; ++j) {
-      const int s = j % STAGES;
-      const bool free_ok = j < STAGES || mbar_wait(y_empty + 8 * s, ((j / STAGES) - 1) & 1, status, abort_flag);
-      __syncwarp();
-      if (!free_ok) break;
-      const int q0 = q_begin + j * BQ;
-      const uint32_t qb = sb + L::OFF_Q + s * L::STAGE;
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::OFF_BAR + L::BAR_SLOT);
+  if (warp >= DS_WARPS) {
+    setmaxnreg_dec_other();
+    if (warp == PRODUCER_WARP) {
+      // ------------------------------------------------------------------ TMA producer
       if (lane == 0) {
-        mbar_expect_tx(y_full + 8 * s, 2 * L::QT);
+        mbar_arrive_expect_tx(k_full, 2 * L::KT);
 #pragma unroll
         for (int h = 0; h < D / 64; ++h) {
-          tma_load_3d(qb + h * BQ * 128, &mq1, y_full + 8 * s, h * 64, q0, bh);
-          tma_load_3d(qb + L::QT + h * BQ * 128, &mq2, y_full + 8 * s, h * 64, q0, bh);
+          tma_load_3d(sb + L::OFF_K1 + h * BK * 128, &mk1, k_full, h * 64, k0, bh);
+          tma_load_3d(sb + L::OFF_K2 + h * BK * 128, &mk2, k_full, h * 64, k0, bh);
         }
-      }
-      float* vals = reinterpret_cast<float*>(smem + L::OFF_VALS + s * 4 * BQ * 4);
+        int issued = 0;
+        for (int j = 0; j < n_yt; ++j) {
+          const int s = j % STAGES;
+          if (j >= STAGES && !mbar_wait(y_empty + 8 * s, ((j / STAGES) - 1) & 1, status, abort_flag)) break;
+          const int q0 = q_begin + j * BQ;
+          const uint32_t qb = sb + L::OFF_Q + s * L::STAGE;
+          mbar_arrive_expect_tx(y_full + 8 * s, 2 * L::QT);
 #pragma unroll
-      for (int k = 0; k < BQ / 32; ++k) {
-        const int qi = lane + 32 * k, q = q0 + qi;
-        const bool in = q < p.NQ;
-        const size_t o = (size_t)bh * p.NQ + q;
-        const float l1v = in ? lse1[o] : 0.f, l2v = in ? lse2[o] : 0.f;
-        vals[qi] = -l1v * kLog2e;
-        vals[BQ + qi] = SETTING == 1 ? -l2v * kLog2e : -(l1v - l2v + (in ? klv[o] : 0.f));
-        vals[2 * BQ + qi] = in ? gv[o] : 0.f;
-      }
-      mbar_arrive(y_full + 8 * s);
-      issued = j + 1;
-    }
-    if (lane == 0) {
-      mbar_drain(k_full, 0, status);
-      for (int j = max(0, issued - STAGES); j < issued; ++j)
-        mbar_drain(y_full + 8 * (j % STAGES), (j / STAGES) & 1, status);
-    }
-    __syncwarp();
-  } else if (warp == MMA_WARP) {
-    // ------------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t id_s = idesc_bf16(BK, BQ, false, false);
-      constexpr uint32_t id_dk = idesc_bf16(BK, D, false, true);
-      constexpr uint32_t id_dq = idesc_bf16(128, BQ, true, true);
-      const uint32_t kopt = sb + (SETTING == 1 ? L::OFF_K2 : L::OFF_K1);
-      const uint64_t k1d = sdesc_sw128(sb + L::OFF_K1, 0, 1024), k2d = sdesc_sw128(sb + L::OFF_K2, 0, 1024);
-      const uint64_t kod = sdesc_sw128(kopt, D == 128 ? BK * 128 : 0, 1024);
-      bool ok = mbar_wait(k_full, 0, status, abort_flag);
-      for (int j = 0; ok && j <= n_yt; ++j) {
-        if (j < n_yt) {
-          const int s = j % STAGES, b = j & 1;
-          if (!mbar_wait(y_full + 8 * s, (j / STAGES) & 1, status, abort_flag)) break;
-          if (j >= 2 && !mbar_wait(s_free + 8 * b, ((j >> 1) - 1) & 1, status, abort_flag)) break;
-          tc_fence_after();
-          const uint32_t q1 = sb + L::OFF_Q + s * L::STAGE, q2 = q1 + L::QT;
-          const uint64_t q1d = sdesc_sw128(q1, 0, 1024), q2d = sdesc_sw128(q2, 0, 1024);
-#pragma unroll
-          for (int ks = 0; ks < D / 16; ++ks) {
-            const uint32_t ka = (ks >> 2) * (BK * 128) + (ks & 3) * 32;  // 128-key tile halves
-            const uint32_t qa = (ks >> 2) * (BQ * 128) + (ks & 3) * 32;  // 64-query tile halves
-            mma_ss(tmem + 128 * b, sdesc_add(k1d, ka), sdesc_add(q1d, qa), id_s, ks > 0);
+          for (int h = 0; h < D / 64; ++h) {
+            tma_load_3d(qb + h * BQ * 128, &mq1, y_full + 8 * s, h * 64, q0, bh);
+            tma_load_3d(qb + L::QT + h * BQ * 128, &mq2, y_full + 8 * s, h * 64, q0, bh);
           }
-#pragma unroll
-          for (int ks = 0; ks < D / 16; ++ks) {
-            const uint32_t ka = (ks >> 2) * (BK * 128) + (ks & 3) * 32;
-            const uint32_t qa = (ks >> 2) * (BQ * 128) + (ks & 3) * 32;
-            mma_ss(tmem + 128 * b + 64, sdesc_add(k2d, ka), sdesc_add(q2d, qa), id_s, ks > 0);
-          }
-          mma_commit(s_full + 8 * b);
+          issued = j + 1;
         }
-        if (j >= 1) {
-          const int jj = j - 1, b = jj & 1, s = jj % STAGES;
-          if (!mbar_wait(ds_full + 8 * b, (jj >> 1) & 1, status, abort_flag)) break;
-          if (jj >= 2 && !mbar_wait(dq_free + 8 * b, ((jj >> 1) - 1) & 1, status, abort_flag)) break;
-          tc_fence_after();
-          // dK += dS^T Q_opt: A = packed dS^T in TMEM (query k-steps 0,1 at columns 128b + 0.., 2,3 at 128b + 32..)
-          const uint64_t qod = sdesc_sw128(sb + L::OFF_Q + s * L::STAGE + (SETTING == 1 ? L::QT : 0), BQ * 128, 1024);
-#pragma unroll
-          for (int ks = 0; ks < BQ / 16; ++ks)
-            mma_ts(tmem + kColDK, tmem + 128 * b + (ks >> 1) * 32 + (ks & 1) * 8, sdesc_add(qod, ks * 2048), id_dk,
-                   jj > 0 || ks > 0);
-          // dQp^T = K_opt^T dS: A = K_opt (keys x d) read MN-major, B = dS^T (keys x queries) MN-major
-          const uint64_t dsd = sdesc_sw128(sb + L::OFF_DS + b * L::DS_BYTES, 0, 1024);
-#pragma unroll
-          for (int ks = 0; ks < BK / 16; ++ks)
-            mma_ss(tmem + kColDQ + 64 * b, sdesc_add(kod, ks * 2048), sdesc_add(dsd, ks * 2048), id_dq, ks > 0);
-          mma_commit(y_empty + 8 * s);
-          mma_commit(ds_free + 8 * b);
-          mma_commit(dq_full + 8 * b);
-        }
+        mbar_drain(k_full, 0, status);
+        for (int j = max(0, issued - STAGES); j < issued; ++j)
+          mbar_drain(y_full + 8 * (j % STAGES), (j / STAGES) & 1, status);
       }
-      // all MMAs done (the last dq_full commit covers every earlier MMA)
-      if (n_yt > 0) mbar_drain(dq_full + 8 * ((n_yt - 1) & 1), ((n_yt - 1) >> 1) & 1, status);
+      __syncwarp();
+    } else if (warp == VALS_WARP) {
+      // ------------------------------------------------------------------ per-query values
+      // Loads for tile j are issued before waiting for the dS warps to release the
+      // previous tile's values, so their latency overlaps that wait.
+      constexpr int PER = BQ / 32;
+      float a[PER], b[PER], g[PER];
+      auto fetch = [&](int j) {
+        const int q0 = q_begin + j * BQ;
+#pragma unroll
+        for (int k = 0; k < PER; ++k) {
+          const int q = q0 + lane + 32 * k;
+          const bool in = q < p.NQ;
+          const size_t o = (size_t)bh * p.NQ + (in ? q : 0);
+          const float l1v = in ? lse1[o] : 0.f, l2v = in ? lse2[o] : 0.f;
+          a[k] = -l1v * kLog2e;
+          b[k] = SETTING == 1 ? -l2v * kLog2e : -(l1v - l2v + (in ? klv[o] : 0.f));
+          g[k] = in ? gv[o] : 0.f;
+        }
+      };
+      if (n_yt > 0) fetch(0);
+      for (int j = 0; j < n_yt; ++j) {
+        const bool ok = j == 0 || mbar_wait(v_free, (j - 1) & 1, status, abort_flag);
+        __syncwarp();
+        if (!ok) break;
+#pragma unroll
+        for (int k = 0; k < PER; ++k) {
+          vals[lane + 32 * k] = a[k];
+          vals[BQ + lane + 32 * k] = b[k];
+          vals[2 * BQ + lane + 32 * k] = g[k];
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(v_full);
+        if (j + 1 < n_yt) fetch(j + 1);
+      }
+    } else if (warp == MMA_WARP) {
+      // ------------------------------------------------------------------ MMA issuer
+      if (lane == 0) {
+        constexpr uint32_t id_s = idesc_bf16(BK, BQ, false, false);
+        constexpr uint32_t id_dk = idesc_bf16(BK, D, false, true);
+        constexpr uint32_t id_dq = idesc_bf16(128, BQ, true, true);
+        constexpr uint32_t HI = sdesc_sw128_hi(1024);  // every operand: 8-row atoms 1024 B apart
+        // low descriptor words; K-major operands have no leading offset, MN-major ones
+        // step 64 elements along M/N by one 128-row tile half
+        const uint32_t k1l = sdesc_sw128_lo(sb + L::OFF_K1, 0), k2l = sdesc_sw128_lo(sb + L::OFF_K2, 0);
+        const uint32_t kol = sdesc_sw128_lo(sb + (SETTING == 1 ? L::OFF_K2 : L::OFF_K1), D == 128 ? BK * 128 : 0);
+        const uint32_t dskl = sdesc_sw128_lo(sb + L::OFF_DS, 0);         // dS as A of dK (K-major over queries)
+        const uint32_t dsml = sdesc_sw128_lo(sb + L::OFF_DS, BK * 128);  // dS as B of dQp (MN-major over queries)
+        bool ok = mbar_wait(k_full, 0, status, abort_flag);
+        for (int j = 0; ok && j <= n_yt; ++j) {
+          if (j < n_yt) {
+            const int s = j % STAGES;
+            if (!mbar_wait(y_full + 8 * s, (j / STAGES) & 1, status, abort_flag)) break;
+            if (j >= 1 && !mbar_wait(s_free, (j - 1) & 1, status, abort_flag)) break;
+            tc_fence_after();
+            const uint32_t q1l = sdesc_sw128_lo(sb + L::OFF_Q + s * L::STAGE, 0), q2l = q1l + (L::QT >> 4);
+#pragma unroll
+            for (int ks = 0; ks < D / 16; ++ks) {
+              const uint32_t ka = ((ks >> 2) * (BK * 128) + (ks & 3) * 32) >> 4;  // 128-key tile halves
+              const uint32_t qa = ((ks >> 2) * (BQ * 128) + (ks & 3) * 32) >> 4;  // 128-query tile halves
+              mma_ss_lohi(tmem + kColS1, k1l + ka, HI, q1l + qa, HI, id_s, ks > 0);
+            }
+#pragma unroll
+            for (int ks = 0; ks < D / 16; ++ks) {
+              const uint32_t ka = ((ks >> 2) * (BK * 128) + (ks & 3) * 32) >> 4;
+              const uint32_t qa = ((ks >> 2) * (BQ * 128) + (ks & 3) * 32) >> 4;
+              mma_ss_lohi(tmem + kColS2, k2l + ka, HI, q2l + qa, HI, id_s, ks > 0);
+            }
+            mma_commit(s_full);
+          }
+          if (j >= 1) {
+            const int jj = j - 1, s = jj % STAGES;
+            // dS(jj) in smem, and dQp^T of tile jj - 1 drained from TMEM
+            if (!mbar_wait(ds_full, jj & 1, status, abort_flag)) break;
+            tc_fence_after();
+            // dK += dS^T Q_opt: A = dS[key][query] K-major (query k-steps), B = Q_opt read MN-major
+            const uint32_t qol =
+                sdesc_sw128_lo(sb + L::OFF_Q + s * L::STAGE + (SETTING == 1 ? L::QT : 0), BQ * 128);
+#pragma unroll
+            for (int ks = 0; ks < BQ / 16; ++ks)
+              mma_ss_lohi(tmem + kColDK, dskl + (((ks >> 2) * (BK * 128) + (ks & 3) * 32) >> 4), HI,
+                          qol + ks * (2048 >> 4), HI, id_dk, jj > 0 || ks > 0);
+            // dQp^T = K_opt^T dS: A = K_opt (keys x d) read MN-major, B = dS (keys x queries) MN-major
+#pragma unroll
+            for (int ks = 0; ks < BK / 16; ++ks)
+              mma_ss_lohi(tmem + kColDQ, kol + ks * (2048 >> 4), HI, dsml + ks * (2048 >> 4), HI, id_dq, ks > 0);
+            mma_commit(y_empty + 8 * s);
+            mma_commit(ds_free);
+          }
+        }
+        // every MMA done: arrives on all_done (waited by the dK epilogue and below)
+        mma_commit(all_done);
+        mbar_drain(all_done, 0, status);
+      }
+      __syncwarp();
     }
-    __syncwarp();
-  } else if (warp < DS_WARPS) {
+  } else {
+    setmaxnreg_inc_ds();
     // ------------------------------------------------------------------ dS warps
     const int grp = warp >> 2, wq = warp & 3;
     const int r = wq * 32 + lane;
     const int key = k0 + r;
+    const int d = r;  // as the reader of dQp^T, lane r holds column d = r
     const float c = p.c;
     const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
+    const uint32_t dsb = sb + L::OFF_DS;
+    // dq_acc[q, d] += dQp^T[d, q] for this warp's 32 queries [32 grp, 32 grp + 32) of tile jt
+    auto add_dq = [&](int jt, const uint32_t(&v)[32]) {
+      const int q0 = q_begin + jt * BQ + grp * 32;
+      if (d < D) {
+        float* base = dq_acc + ((size_t)bh * p.NQ + q0) * D + d;
+        red_rows<D>(base, v, min(32, p.NQ - q0), std::make_integer_sequence<int, 32>{});
+      }
+    };
     for (int j = 0; j < n_yt; ++j) {
-      const int b = j & 1, s = j % STAGES;
-      bool got = mbar_wait(s_full + 8 * b, (j >> 1) & 1, status, abort_flag);
+      bool got = mbar_wait(s_full, j & 1, status, abort_flag);
       __syncwarp();
       if (!got) break;
       tc_fence_after();
-      // the per-query values were staged by the producer lanes: acquire them directly
-      got = mbar_wait(y_full + 8 * s, (j / STAGES) & 1, status, abort_flag);
-      __syncwarp();
-      if (!got) break;
-      uint32_t a[32], bb[32];
-      const uint32_t ta = tmem + lane_base + 128 * b + grp * 32;
-      tmem_ld32(ta, a);
-      tmem_ld32(ta + 64, bb);
-      tmem_ld_wait();
-      reg_fence32(a);
-      reg_fence32(bb);
       const int q0 = q_begin + j * BQ + grp * 32;
-      const float* vals = reinterpret_cast<const float*>(smem + L::OFF_VALS + s * 4 * BQ * 4) + grp * 32;
       const bool masked = (q0 + 31 >= p.NQ) || (key >= p.NK) || (p.causal && key > q0 + p.off);
       uint32_t pk[16];
-      if (masked)
-        make_dst<SETTING, true>(a, bb, pk, c, p.scale, vals, key, q0, p.NQ, p.NK, p.off, p.causal);
-      else
-        make_dst<SETTING, false>(a, bb, pk, c, p.scale, vals, key, q0, p.NQ, p.NK, p.off, p.causal);
-      // the smem copy of dS^T (B of the dQ MMA) is free once the dQ MMA of tile j-2 is done
-      if (j >= 2) {
-        got = mbar_wait(ds_free + 8 * b, ((j >> 1) - 1) & 1, status, abort_flag);
+      // Two halves of 16 query columns: the second half is read after the first
+      // is computed, and TMEM is released once both are in registers.
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t a[16], bb[16];
+        tmem_ld16(tmem + lane_base + kColS1 + grp * 32 + 16 * h, a);
+        tmem_ld16(tmem + lane_base + kColS2 + grp * 32 + 16 * h, bb);
+        tmem_ld_wait();
+        reg_fence16(a);
+        reg_fence16(bb);
+        if (h == 1) {
+          // S of this tile is in registers: the next tile's S MMA may overwrite TMEM
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(s_free);
+        } else {
+          got = mbar_wait(v_full, j & 1, status, abort_flag);
+          __syncwarp();
+          if (!got) break;
+        }
+        const float* vh = vals + grp * 32 + 16 * h;
+        if (masked)
+          make_dst<SETTING, true, 16>(a, bb, pk + 8 * h, c, p.scale, vh,
+                                      visible_cols<16>(key, q0 + 16 * h, p.NQ, p.NK, p.off, p.causal));
+        else
+          make_dst<SETTING, false, 16>(a, bb, pk + 8 * h, c, p.scale, vh, 0u);
+        if (h == 0)  // first half final before the second half is read
+          asm volatile("" : "+r"(pk[0]), "+r"(pk[1]), "+r"(pk[2]), "+r"(pk[3]), "+r"(pk[4]), "+r"(pk[5]),
+                       "+r"(pk[6]), "+r"(pk[7])::"memory");
+      }
+      if (!got) break;
+      // dS is final here: keeps the compiler from sinking its arithmetic below the
+      // TMEM read of dQp^T, where S and the dQp^T block would both be live
+      reg_fence16(pk);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(v_free);
+      // The dK and dQp MMAs of the previous tile are done: dS smem is free and
+      // that tile's dQp^T is complete in TMEM.  Read this warp's block of it
+      // before publishing dS(j), which lets the next dQp MMA overwrite it.
+      if (j >= 1) {
+        got = mbar_wait(ds_free, (j - 1) & 1, status, abort_flag);
         __syncwarp();
         if (!got) break;
       }
-      const uint32_t dsb = sb + L::OFF_DS + b * L::DS_BYTES;
 #pragma unroll
       for (int cch = 0; cch < 4; ++cch) {
         const uint32_t dst = sw128<BK>(dsb, r, grp * 4 + cch);
@@ -308,73 +403,46 @@ __global__ void __launch_bounds__(THREADS, 1)
                      : "memory");
       }
       fence_async_smem();
-      // packed dS^T over this group's first 16 S1^T columns (already read): A of the dK MMA
-      tmem_st16(tmem + lane_base + 128 * b + grp * 32, pk);
-      tmem_st_wait();
+      uint32_t v[32];
+      if (j >= 1) {
+        tc_fence_after();
+        tmem_ld32(tmem + lane_base + kColDQ + grp * 32, v);
+        tmem_ld_wait();
+        reg_fence32(v);
+      }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(s_free + 8 * b);
-        mbar_arrive(ds_full + 8 * b);
-      }
+      if (lane == 0) mbar_arrive(ds_full);
+      if (j >= 1) add_dq(j - 1, v);
     }
-    // ---- dK out
-    constexpr int HALF = D / 2;
-    bool got = mbar_wait(dq_full + 8 * ((n_yt - 1) & 1), ((n_yt - 1) >> 1) & 1, status, abort_flag);
+    // ---- last tile's dQp^T, then dK out (group g writes d columns [32g, 32g + 32))
+    const bool done = mbar_wait(all_done, 0, status, abort_flag);
     __syncwarp();
-    if (got) {
+    if (done) {
       tc_fence_after();
-      uint32_t g0[32], g1[32];
-      const uint32_t tg = tmem + lane_base + kColDK + grp * HALF;
-      tmem_ld32(tg, g0);
-      if (HALF == 64) tmem_ld32(tg + 32, g1);
+      uint32_t v[32];
+      tmem_ld32(tmem + lane_base + kColDQ + grp * 32, v);
+      tmem_ld_wait();
+      reg_fence32(v);
+      add_dq(n_yt - 1, v);
+    }
+    if (done && grp * 32 < D) {
+      uint32_t g0[32];
+      tmem_ld32(tmem + lane_base + kColDK + grp * 32, g0);
       tmem_ld_wait();
       reg_fence32(g0);
-      reg_fence32(g1);
       if (key < p.NK) {
-        __nv_bfloat16* dst = dk_out + ((size_t)bh * p.NK + key) * D + grp * HALF;
+        __nv_bfloat16* dst = dk_out + ((size_t)bh * p.NK + key) * D + grp * 32;
 #pragma unroll
-        for (int v = 0; v < HALF / 8; ++v) {
+        for (int v = 0; v < 4; ++v) {
+          const uint32_t* src = &g0[v * 8];
           uint4 o;
-          const uint32_t* src = v < 4 ? &g0[v * 8] : &g1[(v - 4) * 8];
           o.x = pack_bf16(__uint_as_float(src[0]) * p.scale, __uint_as_float(src[1]) * p.scale);
           o.y = pack_bf16(__uint_as_float(src[2]) * p.scale, __uint_as_float(src[3]) * p.scale);
           o.z = pack_bf16(__uint_as_float(src[4]) * p.scale, __uint_as_float(src[5]) * p.scale);
           o.w = pack_bf16(__uint_as_float(src[6]) * p.scale, __uint_as_float(src[7]) * p.scale);
           reinterpret_cast<uint4*>(dst)[v] = o;
         }
-      }
-    }
-  } else {
-    // ------------------------------------------------------------------ dQ warps
-    const int wq = warp - DQ_WARP0;
-    const int d = wq * 32 + lane;  // lane of dQp^T = column d
-    const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
-    for (int j = 0; j < n_yt; ++j) {
-      const int b = j & 1;
-      const bool got = mbar_wait(dq_full + 8 * b, (j >> 1) & 1, status, abort_flag);
-      __syncwarp();
-      if (!got) break;
-      tc_fence_after();
-      uint32_t v0[32], v1[32];
-      tmem_ld32(tmem + lane_base + kColDQ + 64 * b, v0);
-      tmem_ld32(tmem + lane_base + kColDQ + 64 * b + 32, v1);
-      tmem_ld_wait();
-      reg_fence32(v0);
-      reg_fence32(v1);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(dq_free + 8 * b);
-      if (d < D) {
-        const int q0 = q_begin + j * BQ;
-        float* base = dq_acc + ((size_t)bh * p.NQ + q0) * D + d;
-        const int nrow = min(BQ, p.NQ - q0);
-#pragma unroll
-        for (int i = 0; i < 32; ++i)
-          if (i < nrow) red_add_f32(base + (size_t)i * D, __uint_as_float(v0[i]));
-#pragma unroll
-        for (int i = 0; i < 32; ++i)
-          if (32 + i < nrow) red_add_f32(base + (size_t)(32 + i) * D, __uint_as_float(v1[i]));
       }
     }
   }
