@@ -30,6 +30,7 @@
 #include <utility>
 
 #include "common.cuh"
+#include "ds_math.cuh"
 #include "kernels.h"
 #include "tc.cuh"
 
@@ -86,68 +87,6 @@ template <int D, int... I>
 __device__ __forceinline__ void red_rows(float* base, const uint32_t (&v)[32], int nrow,
                                          std::integer_sequence<int, I...>) {
   ((I < nrow ? red_add_at<I * D * 4>(base, __uint_as_float(v[I])) : void()), ...);
-}
-
-// Per-query values staged for a tile, three arrays of BQ floats, folded so the
-// element loop needs one packed FMA per logit:
-//   nA = -LSE1 log2(e)
-//   nB = -LSE2 log2(e)                    (setting 1)
-//        -(LSE1 - LSE2 + KL)              (setting 2; the log ratio minus KL is then
-//                                          scale (S1 - S2) + nB, from logits and LSEs)
-//   G  = g
-// Bit k set iff query column q0 + k (k < N <= 16) sees `key`: the key exists,
-// the query exists, and (causal) key <= query + off.
-template <int N>
-__device__ __forceinline__ uint32_t visible_cols(int key, int q0, int nq, int nk, int off, int causal) {
-  if (key >= nk) return 0u;
-  const int lo = causal ? min(max(key - off - q0, 0), N) : 0;
-  const int hi = min(max(nq - q0, 0), N);
-  return hi > lo ? ((1u << hi) - 1u) & ~((1u << lo) - 1u) : 0u;
-}
-
-template <int SETTING, bool MASKED, int N>
-__device__ __forceinline__ void make_dst(const uint32_t (&a)[N], const uint32_t (&b)[N], uint32_t* pk, float c,
-                                         float scale, const float* vals, uint32_t visible) {
-  // thread = one key; N query columns with their values in vals[*][0..N-1]; with
-  // MASKED, column k contributes only if bit k of `visible` is set
-  const float2 cc = make_float2(c, c), sc = make_float2(scale, scale);
-#pragma unroll
-  for (int i = 0; i < N; i += 4) {
-    const float4 nA4 = *reinterpret_cast<const float4*>(vals + i);
-    const float4 nB4 = *reinterpret_cast<const float4*>(vals + BQ + i);
-    const float4 G4 = *reinterpret_cast<const float4*>(vals + 2 * BQ + i);
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int k = i + 2 * h;
-      const float2 nA = h ? make_float2(nA4.z, nA4.w) : make_float2(nA4.x, nA4.y);
-      const float2 nB = h ? make_float2(nB4.z, nB4.w) : make_float2(nB4.x, nB4.y);
-      const float2 G = h ? make_float2(G4.z, G4.w) : make_float2(G4.x, G4.y);
-      const float2 s1 = make_float2(__uint_as_float(a[k]), __uint_as_float(a[k + 1]));
-      const float2 s2 = make_float2(__uint_as_float(b[k]), __uint_as_float(b[k + 1]));
-      const float2 x1 = ffma2(s1, cc, nA);
-      float2 p1 = make_float2(ex2(x1.x), ex2(x1.y));
-      bool k0 = true, k1 = true;
-      if (MASKED) {
-        k0 = (visible >> k) & 1u;
-        k1 = (visible >> (k + 1)) & 1u;
-        p1.x = k0 ? p1.x : 0.f;
-        p1.y = k1 ? p1.y : 0.f;
-      }
-      float2 ds;
-      if (SETTING == 1) {
-        const float2 x2 = ffma2(s2, cc, nB);
-        float2 p2 = make_float2(ex2(x2.x), ex2(x2.y));
-        if (MASKED) {
-          p2.x = k0 ? p2.x : 0.f;
-          p2.y = k1 ? p2.y : 0.f;
-        }
-        ds = fmul2(G, fsub2(p2, p1));
-      } else {
-        ds = fmul2(fmul2(G, p1), ffma2(sc, fsub2(s1, s2), nB));
-      }
-      pk[k / 2] = pack_bf16(ds.x, ds.y);
-    }
-  }
 }
 
 template <int D, int SETTING>
@@ -373,10 +312,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         const float* vh = vals + grp * 32 + 16 * h;
         if (masked)
-          make_dst<SETTING, true, 16>(a, bb, pk + 8 * h, c, p.scale, vh,
-                                      visible_cols<16>(key, q0 + 16 * h, p.NQ, p.NK, p.off, p.causal));
+          make_ds_cols<SETTING, true, 16, BQ>(a, bb, pk + 8 * h, c, p.scale, vh,
+                                              visible_queries<16>(key, q0 + 16 * h, p.NQ, p.NK, p.off, p.causal));
         else
-          make_dst<SETTING, false, 16>(a, bb, pk + 8 * h, c, p.scale, vh, 0u);
+          make_ds_cols<SETTING, false, 16, BQ>(a, bb, pk + 8 * h, c, p.scale, vh, 0u);
         if (h == 0)  // first half final before the second half is read
           asm volatile("" : "+r"(pk[0]), "+r"(pk[1]), "+r"(pk[2]), "+r"(pk[3]), "+r"(pk[4]), "+r"(pk[5]),
                        "+r"(pk[6]), "+r"(pk[7])::"memory");

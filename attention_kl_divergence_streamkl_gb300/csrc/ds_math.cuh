@@ -1,0 +1,109 @@
+// Element-wise dS of the attention-KL backward, shared by the fused and the
+// separate tcgen05 kernels.
+//
+// StreamKL technical summary (gist.science/ja/paper/2606.20005), sections 手法 2
+// "recompute strategy" (P_t = exp(S_t - LSE_t) rebuilt per tile) and 手法 3
+// "numerical stability" (the setting-2 log ratio from logits and saved LSEs).
+// With L = sum_i g_i KL_i (chain rule, derived):
+//     setting 1:  dS2 = g (P2 - P1)
+//     setting 2:  dS1 = g P1 (r - KL),  r = (S1 - LSE1) - (S2 - LSE2)
+// Per-query values are folded so that each logit needs one packed FMA, in log2
+// units (c = scale log2(e)):
+//     nA = -LSE1 log2(e)
+//     nB = -LSE2 log2(e)                 (setting 1)
+//          -(LSE1 - LSE2 + KL)           (setting 2: r - KL = scale (S1 - S2) + nB)
+//     G  = g
+// so P1 = 2^(c S1 + nA), P2 = 2^(c S2 + nB).
+#pragma once
+
+#include "common.cuh"
+
+namespace skl {
+
+// Bit k set iff query column q0 + k (k < N <= 16) sees `key`: the key exists,
+// the query exists, and (causal) key <= query + off.
+template <int N>
+__device__ __forceinline__ uint32_t visible_queries(int key, int q0, int nq, int nk, int off, int causal) {
+  if (key >= nk) return 0u;
+  const int lo = causal ? min(max(key - off - q0, 0), N) : 0;
+  const int hi = min(max(nq - q0, 0), N);
+  return hi > lo ? ((1u << hi) - 1u) & ~((1u << lo) - 1u) : 0u;
+}
+
+// Bit k set iff key column k0 + k (k < N <= 16) is seen by query `q`.
+template <int N>
+__device__ __forceinline__ uint32_t visible_keys(int q, int k0, int nq, int nk, int off, int causal) {
+  if (q >= nq) return 0u;
+  const int kend = causal ? min(nk, q + off + 1) : nk;
+  const int hi = min(max(kend - k0, 0), N);
+  return hi > 0 ? (1u << hi) - 1u : 0u;
+}
+
+// One dS element pair from the two logit pairs and the folded values; with
+// MASKED, an element whose bit in `visible` (at position k, k + 1) is clear is 0.
+template <int SETTING, bool MASKED>
+__device__ __forceinline__ uint32_t ds_pair(float2 s1, float2 s2, float2 cc, float2 sc, float2 nA, float2 nB,
+                                            float2 G, uint32_t visible, int k) {
+  const float2 x1 = ffma2(s1, cc, nA);
+  float2 p1 = make_float2(ex2(x1.x), ex2(x1.y));
+  bool k0 = true, k1 = true;
+  if (MASKED) {
+    k0 = (visible >> k) & 1u;
+    k1 = (visible >> (k + 1)) & 1u;
+    p1.x = k0 ? p1.x : 0.f;
+    p1.y = k1 ? p1.y : 0.f;
+  }
+  float2 ds;
+  if (SETTING == 1) {
+    const float2 x2 = ffma2(s2, cc, nB);
+    float2 p2 = make_float2(ex2(x2.x), ex2(x2.y));
+    if (MASKED) {
+      p2.x = k0 ? p2.x : 0.f;
+      p2.y = k1 ? p2.y : 0.f;
+    }
+    ds = fmul2(G, fsub2(p2, p1));
+  } else {
+    ds = fmul2(fmul2(G, p1), ffma2(sc, fsub2(s1, s2), nB));
+  }
+  return pack_bf16(ds.x, ds.y);
+}
+
+// Thread = one key, N query columns with their folded values in vals[0..N),
+// vals[VSTRIDE..), vals[2 VSTRIDE..) (nA, nB, G); dS packed as bf16 pairs.
+template <int SETTING, bool MASKED, int N, int VSTRIDE>
+__device__ __forceinline__ void make_ds_cols(const uint32_t (&a)[N], const uint32_t (&b)[N], uint32_t* pk, float c,
+                                             float scale, const float* vals, uint32_t visible) {
+  const float2 cc = make_float2(c, c), sc = make_float2(scale, scale);
+#pragma unroll
+  for (int i = 0; i < N; i += 4) {
+    const float4 nA4 = *reinterpret_cast<const float4*>(vals + i);
+    const float4 nB4 = *reinterpret_cast<const float4*>(vals + VSTRIDE + i);
+    const float4 G4 = *reinterpret_cast<const float4*>(vals + 2 * VSTRIDE + i);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int k = i + 2 * h;
+      const float2 nA = h ? make_float2(nA4.z, nA4.w) : make_float2(nA4.x, nA4.y);
+      const float2 nB = h ? make_float2(nB4.z, nB4.w) : make_float2(nB4.x, nB4.y);
+      const float2 G = h ? make_float2(G4.z, G4.w) : make_float2(G4.x, G4.y);
+      const float2 s1 = make_float2(__uint_as_float(a[k]), __uint_as_float(a[k + 1]));
+      const float2 s2 = make_float2(__uint_as_float(b[k]), __uint_as_float(b[k + 1]));
+      pk[k / 2] = ds_pair<SETTING, MASKED>(s1, s2, cc, sc, nA, nB, G, visible, k);
+    }
+  }
+}
+
+// Thread = one query row with its folded values (nA, nB, G), N key columns.
+template <int SETTING, bool MASKED, int N>
+__device__ __forceinline__ void make_ds_row(const uint32_t (&a)[N], const uint32_t (&b)[N], uint32_t* pk, float c,
+                                            float scale, float nAr, float nBr, float Gr, uint32_t visible) {
+  const float2 cc = make_float2(c, c), sc = make_float2(scale, scale);
+  const float2 nA = make_float2(nAr, nAr), nB = make_float2(nBr, nBr), G = make_float2(Gr, Gr);
+#pragma unroll
+  for (int k = 0; k < N; k += 2) {
+    const float2 s1 = make_float2(__uint_as_float(a[k]), __uint_as_float(a[k + 1]));
+    const float2 s2 = make_float2(__uint_as_float(b[k]), __uint_as_float(b[k + 1]));
+    pk[k / 2] = ds_pair<SETTING, MASKED>(s1, s2, cc, sc, nA, nB, G, visible, k);
+  }
+}
+
+}  // namespace skl
