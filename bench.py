@@ -238,7 +238,12 @@ def run_reference(args):
     line = {"impl": "reference", "metric": metric, "value": value, "unit": unit, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": w.name, "sample_rows": R},
+            "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "N_Q": w.NQ, "N_K": w.NK, "D": w.D,
+                       "causal": w.causal, "setting": args.setting if not decode else None,
+                       "path": ("oracle rows_forward" if decode else "oracle rows_forward + head_backward_rows"),
+                       "per_gpu_units": "a bounded sample of the workload per step (see cpu_baseline.sample)",
+                       "parallelism": "replicas1"},
             "cpu_baseline": {"value": value, "unit": unit, "cores": cpu_cores(), "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
