@@ -72,23 +72,23 @@ streamkl_status status_ptr(int** out) {
 
 streamkl_status from_cuda(cudaError_t e) { return e == cudaSuccess ? STREAMKL_OK : STREAMKL_ERR_CUDA; }
 
-size_t dq_acc_bytes(const Problem& p) { return (size_t)p.BH * p.NQ * p.D * sizeof(float); }
+size_t fused_acc_bytes(const Problem& p) { return (size_t)p.BH * p.NK * p.D * sizeof(float); }
 
-// The fused path adds dQ partials into the fp32 buffer with atomics; they stay
+// The fused path adds dK partials into the fp32 buffer with atomics; they stay
 // cheap while the rows being accumulated stay in L2.  Its blocks run head by
-// head (all key tiles of one (b, h) before the next), so the live part of the
-// buffer is the dQ rows of the heads that are in flight at once: one head's
-// N_Q x D fp32 rows times the heads a full wave of blocks spans.
-size_t live_dq_bytes(const Problem& p, int num_sms) {
-  const long long key_tiles = (p.NK + 127) / 128;  // blocks per head
-  const long long heads_in_flight = (num_sms + key_tiles - 1) / key_tiles + 1;
+// head (all query tiles of one (b, h) before the next), so the live part of the
+// buffer is the dK rows of the heads that are in flight at once: one head's
+// N_K x D fp32 rows times the heads a full wave of blocks spans.
+size_t live_acc_bytes(const Problem& p, int num_sms) {
+  const long long query_tiles = (p.NQ + 127) / 128;  // blocks per head
+  const long long heads_in_flight = (num_sms + query_tiles - 1) / query_tiles + 1;
   const long long heads = heads_in_flight < p.BH ? heads_in_flight : p.BH;
-  return (size_t)p.NQ * p.D * sizeof(float) * (size_t)heads;
+  return (size_t)p.NK * p.D * sizeof(float) * (size_t)heads;
 }
 
 int resolve_bwd_mode(const Problem& p, int mode, size_t l2_bytes, int num_sms) {
   if (mode == STREAMKL_BWD_FUSED || mode == STREAMKL_BWD_SEPARATE) return mode;
-  return live_dq_bytes(p, num_sms) <= l2_bytes ? STREAMKL_BWD_FUSED : STREAMKL_BWD_SEPARATE;
+  return live_acc_bytes(p, num_sms) <= l2_bytes ? STREAMKL_BWD_FUSED : STREAMKL_BWD_SEPARATE;
 }
 
 streamkl_status device_l2_bytes(size_t* out) {
@@ -250,7 +250,7 @@ streamkl_status streamkl_bwd_workspace(streamkl_shape s, int bwd_mode, size_t* b
     if ((v = device_l2_bytes(&l2)) != STREAMKL_OK || (v = device_sms(&sms)) != STREAMKL_OK) return v;
     bwd_mode = resolve_bwd_mode(p, bwd_mode, l2, sms);
   }
-  *bytes = bwd_mode == STREAMKL_BWD_FUSED ? dq_acc_bytes(p) : 0;
+  *bytes = bwd_mode == STREAMKL_BWD_FUSED ? fused_acc_bytes(p) : 0;
   return STREAMKL_OK;
 }
 
@@ -281,7 +281,7 @@ static streamkl_status bwd_common(int setting, const void* q1, const void* k1, c
     bwd_mode = resolve_bwd_mode(p, bwd_mode, l2, sms);
   }
   if (bwd_mode == STREAMKL_BWD_FUSED &&
-      (!workspace || !aligned16(workspace) || workspace_bytes < dq_acc_bytes(p)))
+      (!workspace || !aligned16(workspace) || workspace_bytes < fused_acc_bytes(p)))
     return STREAMKL_ERR_WORKSPACE;
   int* status = nullptr;
   if ((v = status_ptr(&status)) != STREAMKL_OK) return v;

@@ -61,7 +61,7 @@ typedef struct {
 
 /* Backward path selection (the adaptive rule of section 手法 2 "kernel fusion"). */
 typedef enum {
-  STREAMKL_BWD_AUTO = 0,     /* fused when the live rows of the fp32 dQ buffer fit in L2, else separate */
+  STREAMKL_BWD_AUTO = 0,     /* fused when the live rows of the fp32 dK buffer fit in L2, else separate */
   STREAMKL_BWD_FUSED = 1,    /* one pass over each QK tile pair, dQ by atomics into fp32 */
   STREAMKL_BWD_SEPARATE = 2, /* a Q-stationary dQ kernel and a K-stationary dK kernel */
   STREAMKL_BWD_DQ_ONLY = 3,  /* separate path, dQ kernel only (dK pointer may be NULL) */
@@ -127,17 +127,18 @@ streamkl_status streamkl_fwd_splitk_noalloc(const void* q1, const void* k1, cons
                                             float* lse2, void* stream);
 
 /*
- * Backward workspace: fused mode needs an fp32 [B,H,N_Q,D] dQ accumulator
- * (zeroed by the library); separate mode needs none (0 bytes).  AUTO resolves
- * with the current device's L2 size.
+ * Backward workspace: fused mode needs an fp32 [B,H,N_K,D] dK accumulator
+ * (zeroed by the library; the fused kernel keeps dQ on chip and adds dK
+ * partials here); separate mode needs none (0 bytes).  AUTO resolves with the
+ * current device's L2 size.
  */
 streamkl_status streamkl_bwd_workspace(streamkl_shape s, int bwd_mode, size_t* bytes);
 /*
  * Which path AUTO takes on a device with `l2_bytes` of L2 and `num_sms` SMs
  * (pure host rule, no device; 0 for an invalid shape).  Fused iff the live part
- * of the fp32 dQ buffer fits in L2: the fused blocks run head by head, so that
- * is one head's N_Q x D x 4 bytes times the heads a wave of num_sms blocks
- * (128 keys each) spans, plus one.
+ * of the fp32 dK buffer fits in L2: the fused blocks run head by head, so that
+ * is one head's N_K x D x 4 bytes times the heads a wave of num_sms blocks
+ * (128 queries each) spans, plus one.
  */
 int streamkl_bwd_select(streamkl_shape s, size_t l2_bytes, int num_sms);
 

@@ -107,9 +107,9 @@ def test_workspace_sizes(lib):
     assert n.value == 8 * 32 * 4 * 19 * 5 * 4
     s16 = K.make_shape(8, 32, 17, 131072, 128)
     assert lib.streamkl_fwd_splitk_workspace(s16, 19, ctypes.byref(n)) == K.ERR_UNSUPPORTED
-    s = K.make_shape(2, 32, 4096, 4096, 128)
+    s = K.make_shape(2, 32, 4096, 8192, 128)  # fused: fp32 dK accumulator [B, H, N_K, D]
     assert lib.streamkl_bwd_workspace(s, K.BWD_FUSED, ctypes.byref(n)) == K.OK
-    assert n.value == 2 * 32 * 4096 * 128 * 4
+    assert n.value == 2 * 32 * 8192 * 128 * 4
     assert lib.streamkl_bwd_workspace(s, K.BWD_SEPARATE, ctypes.byref(n)) == K.OK
     assert n.value == 0
     for mode in (K.BWD_DQ_ONLY, K.BWD_DK_ONLY):
@@ -150,13 +150,13 @@ def test_splitk_plan_minimises_the_wave_model(lib, bh, nk, sms):
 
 
 def _live_rows_bytes(B, H, NQ, NK, D, sms):
-    key_tiles = -(-NK // 128)
-    heads = min(B * H, -(-sms // key_tiles) + 1)
-    return NQ * D * 4 * heads
+    query_tiles = -(-NQ // 128)
+    heads = min(B * H, -(-sms // query_tiles) + 1)
+    return NK * D * 4 * heads
 
 
 def test_bwd_select_rule(lib):
-    # fused exactly while the live dQ rows (heads in flight x N_Q x D x 4 B) fit in L2
+    # fused exactly while the live dK rows (heads in flight x N_K x D x 4 B) fit in L2
     l2, sms = 135528448, 152  # GB300
     assert K.bwd_select(1, 1, 128, 128, 64, l2, sms) == K.BWD_FUSED
     assert K.bwd_select(2, 32, 4096, 4096, 128, l2, sms) == K.BWD_FUSED  # whole buffer 128 MiB; live 12 MiB
@@ -165,9 +165,9 @@ def test_bwd_select_rule(lib):
     for n in (100000, 120000, 131072, 140000, 200000):
         want = K.BWD_FUSED if _live_rows_bytes(1, 8, n, n, 128, sms) <= l2 else K.BWD_SEPARATE
         assert K.bwd_select(1, 8, n, n, 128, l2, sms) == want, n
-    # few key tiles: a wave spans many heads, all of whose rows are live
-    assert _live_rows_bytes(64, 32, 4096, 256, 128, sms) == 4096 * 128 * 4 * 77
-    assert K.bwd_select(64, 32, 4096, 256, 128, 77 * 4096 * 512, sms) == K.BWD_FUSED
-    assert K.bwd_select(64, 32, 4096, 256, 128, 77 * 4096 * 512 - 1, sms) == K.BWD_SEPARATE
+    # few query tiles: a wave spans many heads, all of whose rows are live
+    assert _live_rows_bytes(64, 32, 256, 4096, 128, sms) == 4096 * 128 * 4 * 77
+    assert K.bwd_select(64, 32, 256, 4096, 128, 77 * 4096 * 512, sms) == K.BWD_FUSED
+    assert K.bwd_select(64, 32, 256, 4096, 128, 77 * 4096 * 512 - 1, sms) == K.BWD_SEPARATE
     assert K.bwd_select(0, 1, 8, 8, 64, l2, sms) == 0  # invalid shape
     assert K.bwd_select(1, 1, 8, 8, 64, l2, 0) == 0  # no SM count
