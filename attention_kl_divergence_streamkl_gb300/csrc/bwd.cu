@@ -23,8 +23,9 @@
 // LSU.  dKp^T is double-buffered so they have two tile periods per tile.
 //   warps 0-15  dS warps: thread = query row (lane quarter = warp % 4), group g = warp / 4
 //               takes key columns [32g, 32g + 32); at the end they write dQ
-//   warp 16     TMA producer (Q1, Q2 once; K_opt and the other K tile through two slots each)
+//   warp 16     TMA producer: Q1, Q2 once, the other K tile through two slots
 //   warp 17     TMEM owner and MMA issuer
+//   warp 18     TMA producer of K_opt (two slots, each held until the gradient MMAs)
 //   warps 20-23 dK warps: thread = column d of dKp^T, reduce-add into dk_acc
 // Warpgroups 4-5 give registers to the dS warpgroups (setmaxnreg).
 #include <utility>
@@ -43,6 +44,7 @@ constexpr int SLOTS = 2;  // per streamed K tensor
 constexpr int DS_WARPS = 16;
 constexpr int PRODUCER_WARP = 16;
 constexpr int MMA_WARP = 17;
+constexpr int KOPT_WARP = 18;
 constexpr int DK_WARP0 = 20;
 constexpr int THREADS = 24 * 32;
 constexpr int kRegsDs = 88, kRegsOther = 64;  // 512 * 88 + 256 * 64 = 768 * 80 registers at launch
@@ -161,28 +163,38 @@ __global__ void __launch_bounds__(THREADS, 1)
           tma_load_3d(sb + L::OFF_Q2 + h * BQ * 128, &mq2, q_full, h * 64, q0, bh);
         }
         const CUtensorMap* mka = SETTING == 1 ? &mk1 : &mk2;
-        const CUtensorMap* mkb = SETTING == 1 ? &mk2 : &mk1;
-        int issued_t = 0, issued_o = 0;
+        int issued = 0;
         for (int j = 0; j < n_kt; ++j) {
-          const int s = j % SLOTS, k0 = j * BK;
-          // the other K tile first: S_a is issued first and frees it first
+          const int s = j % SLOTS;
           if (j >= SLOTS && !mbar_wait(kt_empty + 8 * s, ((j / SLOTS) - 1) & 1, status, abort_flag)) break;
           mbar_arrive_expect_tx(kt_full + 8 * s, L::TK);
 #pragma unroll
           for (int h = 0; h < D / 64; ++h)
-            tma_load_3d(sb + L::OFF_KT + s * L::TK + h * BK * 128, mka, kt_full + 8 * s, h * 64, k0, bh);
-          issued_t = j + 1;
+            tma_load_3d(sb + L::OFF_KT + s * L::TK + h * BK * 128, mka, kt_full + 8 * s, h * 64, j * BK, bh);
+          issued = j + 1;
+        }
+        mbar_drain(q_full, 0, status);
+        for (int j = max(0, issued - SLOTS); j < issued; ++j)
+          mbar_drain(kt_full + 8 * (j % SLOTS), (j / SLOTS) & 1, status);
+      }
+      __syncwarp();
+    } else if (warp == KOPT_WARP) {
+      // ------------------------------------------------------------------ TMA producer of K_opt
+      // A stream of its own: its slots free only after the gradient MMAs, and the
+      // other K tile must not wait behind it.
+      if (lane == 0) {
+        const CUtensorMap* mkb = SETTING == 1 ? &mk2 : &mk1;
+        int issued = 0;
+        for (int j = 0; j < n_kt; ++j) {
+          const int s = j % SLOTS;
           if (j >= SLOTS && !mbar_wait(ko_empty + 8 * s, ((j / SLOTS) - 1) & 1, status, abort_flag)) break;
           mbar_arrive_expect_tx(ko_full + 8 * s, L::TK);
 #pragma unroll
           for (int h = 0; h < D / 64; ++h)
-            tma_load_3d(sb + L::OFF_KO + s * L::TK + h * BK * 128, mkb, ko_full + 8 * s, h * 64, k0, bh);
-          issued_o = j + 1;
+            tma_load_3d(sb + L::OFF_KO + s * L::TK + h * BK * 128, mkb, ko_full + 8 * s, h * 64, j * BK, bh);
+          issued = j + 1;
         }
-        mbar_drain(q_full, 0, status);
-        for (int j = max(0, issued_t - SLOTS); j < issued_t; ++j)
-          mbar_drain(kt_full + 8 * (j % SLOTS), (j / SLOTS) & 1, status);
-        for (int j = max(0, issued_o - SLOTS); j < issued_o; ++j)
+        for (int j = max(0, issued - SLOTS); j < issued; ++j)
           mbar_drain(ko_full + 8 * (j % SLOTS), (j / SLOTS) & 1, status);
       }
       __syncwarp();
