@@ -284,8 +284,9 @@ def run_ours(args):
     stream = torch.cuda.current_stream(dev)
 
     # ---- one step, with an event between kernels so each is timed on its stream
-    def step(qs, ev=None):
+    def step(qs, ev=None, gq=None):
         a, b, c, d = qs
+        g_ = g if gq is None else gq
         if decode:
             out = skl.fwd(a, b, c, d, scale, causal) if args.nonsplit else skl.fwd_splitk(a, b, c, d, scale, causal)
             if ev:
@@ -297,12 +298,12 @@ def run_ours(args):
         bwd = skl.bwd_s1 if args.setting == 1 else skl.bwd_s2
         extra = () if args.setting == 1 else (kl,)
         if mode == skl.BWD_SEPARATE:
-            dq = bwd(a, b, c, d, l1, l2, *extra, g, scale, causal, skl.BWD_DQ_ONLY)[0]
+            dq = bwd(a, b, c, d, l1, l2, *extra, g_, scale, causal, skl.BWD_DQ_ONLY)[0]
             if ev:
                 ev[2].record(stream)
-            dk = bwd(a, b, c, d, l1, l2, *extra, g, scale, causal, skl.BWD_DK_ONLY)[1]
+            dk = bwd(a, b, c, d, l1, l2, *extra, g_, scale, causal, skl.BWD_DK_ONLY)[1]
         else:
-            dq, dk = bwd(a, b, c, d, l1, l2, *extra, g, scale, causal, mode)
+            dq, dk = bwd(a, b, c, d, l1, l2, *extra, g_, scale, causal, mode)
             if ev:
                 ev[2].record(stream)
         if ev:
@@ -388,15 +389,39 @@ def run_ours(args):
         pinned = [t.pin_memory() for t in host]
         pg = host_g.pin_memory()
         out_host = torch.empty((w.B, w.H, w.NQ), dtype=torch.float32).pin_memory()
+        # Inputs stream in as in a training loop: a copy stream fills one of two device
+        # input sets while the compute stream works on the other.  Every step's
+        # host->device copy and its result's read-back lie inside the timed region.
+        copy_stream = torch.cuda.Stream(dev)
+        bufs = [[torch.empty_like(t, device=dev) for t in pinned] for _ in range(2)]
+        gbufs = [torch.empty_like(pg, device=dev) for _ in range(2)]
+        ready = [torch.cuda.Event() for _ in range(2)]
+        freed = [torch.cuda.Event() for _ in range(2)]
+
+        def load(k):
+            b = k % 2
+            if k >= 2:
+                copy_stream.wait_event(freed[b])  # step k - 2 is done with this set
+            with torch.cuda.stream(copy_stream):
+                for dst, src in zip(bufs[b], pinned):
+                    dst.copy_(src, non_blocking=True)
+                if not decode:
+                    gbufs[b].copy_(pg, non_blocking=True)  # the upstream gradient is a host input too
+            ready[b].record(copy_stream)
+
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize(dev)
         e0.record(stream)
-        for _ in range(args.steps):
-            dqs = [t.to(dev, non_blocking=True) for t in pinned]
-            if not decode:
-                g.copy_(pg, non_blocking=True)  # the upstream gradient is a host input too
-            kl = step(dqs)[0]
+        copy_stream.wait_event(e0)
+        load(0)
+        for k in range(args.steps):
+            b = k % 2
+            if k + 1 < args.steps:
+                load(k + 1)
+            stream.wait_event(ready[b])
+            kl = step(bufs[b], gq=gbufs[b])[0]
             out_host.copy_(kl, non_blocking=True)
+            freed[b].record(stream)
         e1.record(stream)
         torch.cuda.synchronize(dev)
         e2e_ms = e0.elapsed_time(e1) / args.steps
