@@ -7,11 +7,13 @@
 // setting 2 (P2 fixed) optimises Q1/K1; the dS arithmetic (ds_math.cuh) is the
 // fused kernel's.  dQ = scale dS K_opt, dK = scale dS^T Q_opt.
 //
-// One kernel template serves both separate kernels.  A block owns a stationary
-// tile X of 128 rows (query rows for dQ, keys for dK) on the 128 TMEM lanes and
-// streams tiles Y of 128 rows of the other side:
+// In both kernels the 128 TMEM lanes of the logits are queries, so a dS thread
+// owns a query row and holds its folded LSE1, LSE2, g, KL in registers.
+//
+// dQ kernel: a block owns 128 query rows X (Q1, Q2 stationary) and streams key
+// tiles Y:
 //     S1 = X1 Y1^T, S2 = X2 Y2^T          (tcgen05, both operands K-major in smem)
-//     dS from S1, S2 and the folded per-query values, packed to bf16 into TMEM
+//     dS from S1, S2 and the row's values, packed to bf16 into TMEM
 //     G += dS Y_opt                       (tcgen05, A = dS in TMEM, B = Y_opt
 //                                          read MN-major from the same smem tile)
 // so dS never leaves the SM.  TMEM (512 columns): S1 [0,128), S2 [128,256),
@@ -19,13 +21,15 @@
 // logits are single-buffered: the dS warps copy their columns into registers
 // (in two halves) and release them, so S of the next tile is computed while
 // they work.
-//   warps 0-15  dS warps: thread = X row (lane quarter = warp % 4), group g = warp / 4
-//               takes columns [32g, 32g + 32) of each Y tile; then they write G out
+//   warps 0-15  dS warps: thread = query row (lane quarter = warp % 4), group g = warp / 4
+//               takes columns [32g, 32g + 32) of each key tile; then they write dQ out
 //   warp 16     TMA producer: X once; Y_opt (read by the gradient MMA, so held until
 //               it is done) through three slots, the other Y tile through two
 //   warp 17     TMEM owner and MMA issuer; issues S(j) before G += dS(j-1)
-//   warp 18     (dK kernel) stages the per-query values of each Y tile in smem
 // Warpgroup 4 gives registers to the dS warpgroups (setmaxnreg).
+//
+// The dK kernel (bwd_dk_kernel, below) keeps 128 keys stationary and streams
+// query tiles as the M operand of the logits MMA; see its own comment.
 #include "common.cuh"
 #include "ds_math.cuh"
 #include "kernels.h"
@@ -34,12 +38,12 @@
 namespace skl {
 namespace {
 
-constexpr int BX = 128;  // stationary rows (MMA M)
-constexpr int BY = 128;  // streamed rows per tile (MMA N of S, K of the gradient MMA)
+constexpr int BX = 128;  // stationary query rows (MMA M)
+constexpr int BY = 128;  // streamed keys per tile (MMA N of S, K of the gradient MMA)
 constexpr int DS_WARPS = 16;
 constexpr int PRODUCER_WARP = 16;
 constexpr int MMA_WARP = 17;
-constexpr int VALS_WARP = 18;
+constexpr int QOPT_WARP = 18;  // dK kernel: producer of the Q_opt tiles
 constexpr int THREADS = 20 * 32;
 constexpr int kRegsDs = 104, kRegsOther = 64;  // 512 * 104 + 128 * 64 = 640 * 96 registers at launch
 constexpr uint32_t kTmemCols = 512;
@@ -53,11 +57,10 @@ struct Smem {
   static constexpr int OFF_X2 = TILE;
   static constexpr int OFF_YO = 2 * TILE;               // Y_opt slots [YO_SLOTS]
   static constexpr int OFF_YT = OFF_YO + YO_SLOTS * TILE;  // the other Y tile, slots [YT_SLOTS]
-  static constexpr int OFF_VALS = OFF_YT + YT_SLOTS * TILE;  // [3][BY] fp32 (dK kernel), one tile
-  static constexpr int OFF_BAR = OFF_VALS + 3 * BY * 4;
-  // x_full, yo_full[3], yo_empty[3], yt_full[2], yt_empty[2], s_full, s_free, v_full, v_free, ds_full[2],
-  // ds_free[2], g_done; then the TMEM base address slot and the abort flag
-  static constexpr int BAR_SLOT = 8 * 20;
+  static constexpr int OFF_BAR = OFF_YT + YT_SLOTS * TILE;
+  // x_full, yo_full[3], yo_empty[3], yt_full[2], yt_empty[2], s_full, s_free, ds_full[2], ds_free[2],
+  // g_done; then the TMEM base address slot and the abort flag
+  static constexpr int BAR_SLOT = 8 * 18;
   static constexpr int BYTES = OFF_BAR + BAR_SLOT + 16 + 1024;
 };
 static_assert(Smem<128>::BYTES <= 227 * 1024, "shared memory");
@@ -69,9 +72,9 @@ __device__ __forceinline__ void setmaxnreg_dec_other() {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsOther));
 }
 
-template <int D, int SETTING, bool KSTAT>
+template <int D, int SETTING>
 __global__ void __launch_bounds__(THREADS, 1)
-    bwd_tc_kernel(const Problem p, const float* __restrict__ lse1, const float* __restrict__ lse2,
+    bwd_dq_kernel(const Problem p, const float* __restrict__ lse1, const float* __restrict__ lse2,
                   const float* __restrict__ klv, const float* __restrict__ gv, __nv_bfloat16* __restrict__ out,
                   int* status, const __grid_constant__ CUtensorMap mx1, const __grid_constant__ CUtensorMap mx2,
                   const __grid_constant__ CUtensorMap my1, const __grid_constant__ CUtensorMap my2) {
@@ -80,27 +83,19 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint8_t* smem = align1024(smem_raw);
   const uint32_t sb = smem_u32(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // X side: queries (dQ) or keys (dK); Y side: the other
-  const int NX = KSTAT ? p.NK : p.NQ, NY = KSTAT ? p.NQ : p.NK;
+  const int NX = p.NQ, NY = p.NK;
   const int n_xt = (NX + BX - 1) / BX;
   const int bh = blockIdx.x % p.BH;
-  // longest blocks first: for dQ the last query tiles, for dK the first key tiles
-  const int xt = KSTAT ? (int)(blockIdx.x / p.BH) : n_xt - 1 - (int)(blockIdx.x / p.BH);
+  const int xt = n_xt - 1 - (int)(blockIdx.x / p.BH);  // longest blocks (the last query tiles) first
   const int x0 = xt * BX;
-  int y_begin = 0, y_end = NY;
-  if (p.causal) {
-    if (KSTAT) y_begin = max(0, x0 - p.off) / BY * BY;            // first query that sees key x0
-    else y_end = min(p.NK, min(p.NQ, x0 + BX) - 1 + p.off + 1);  // keys the last row sees
-  }
-  const int y_first = y_begin / BY;
-  const int n_yt = (y_end - y_begin + BY - 1) / BY;
+  const int y_end = p.causal ? min(NY, min(NX, x0 + BX) - 1 + p.off + 1) : NY;  // keys the last row sees
+  const int n_yt = (y_end + BY - 1) / BY;
 
   const uint32_t bar = sb + L::OFF_BAR;
   const uint32_t x_full = bar, yo_full = bar + 8, yo_empty = bar + 32, yt_full = bar + 56, yt_empty = bar + 72,
-                 s_full = bar + 88, s_free = bar + 96, v_full = bar + 104, v_free = bar + 112, ds_full = bar + 120,
-                 ds_free = bar + 136, g_done = bar + 152, slot = bar + L::BAR_SLOT;
+                 s_full = bar + 88, s_free = bar + 96, ds_full = bar + 104, ds_free = bar + 120, g_done = bar + 136,
+                 slot = bar + L::BAR_SLOT;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_BAR + L::BAR_SLOT + 4);
-  float* vals = reinterpret_cast<float*>(smem + L::OFF_VALS);
 
   if (threadIdx.x == 0) {
     mbar_init(x_full, 1);
@@ -118,8 +113,6 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     mbar_init(s_full, 1);
     mbar_init(s_free, DS_WARPS);
-    mbar_init(v_full, 1);
-    mbar_init(v_free, DS_WARPS);
     mbar_init(g_done, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -151,7 +144,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int j = 0; j < n_yt; ++j) {
           const int so = j % YO_SLOTS, st = j % YT_SLOTS;
           if (j >= YO_SLOTS && !mbar_wait(yo_empty + 8 * so, ((j / YO_SLOTS) - 1) & 1, status, abort_flag)) break;
-          const int y0 = (y_first + j) * BY;
+          const int y0 = j * BY;
           mbar_arrive_expect_tx(yo_full + 8 * so, L::TILE);
 #pragma unroll
           for (int h = 0; h < D / 64; ++h)
@@ -172,40 +165,6 @@ __global__ void __launch_bounds__(THREADS, 1)
           mbar_drain(yt_full + 8 * (j % YT_SLOTS), (j / YT_SLOTS) & 1, status);
       }
       __syncwarp();
-    } else if (warp == VALS_WARP && KSTAT) {
-      // ------------------------------------------------------------------ per-query values (dK kernel)
-      // Loads for tile j are issued before waiting for the dS warps to release the
-      // previous tile's values, so their latency overlaps that wait.
-      constexpr int PER = BY / 32;
-      float a[PER], b[PER], g[PER];
-      auto fetch = [&](int j) {
-        const int q0 = (y_first + j) * BY;
-#pragma unroll
-        for (int k = 0; k < PER; ++k) {
-          const int q = q0 + lane + 32 * k;
-          const bool in = q < p.NQ;
-          const size_t o = (size_t)bh * p.NQ + (in ? q : 0);
-          const float l1v = in ? lse1[o] : 0.f, l2v = in ? lse2[o] : 0.f;
-          a[k] = -l1v * kLog2e;
-          b[k] = SETTING == 1 ? -l2v * kLog2e : -(l1v - l2v + (in ? klv[o] : 0.f));
-          g[k] = in ? gv[o] : 0.f;
-        }
-      };
-      if (n_yt > 0) fetch(0);
-      for (int j = 0; j < n_yt; ++j) {
-        const bool ok = j == 0 || mbar_wait(v_free, (j - 1) & 1, status, abort_flag);
-        __syncwarp();
-        if (!ok) break;
-#pragma unroll
-        for (int k = 0; k < PER; ++k) {
-          vals[lane + 32 * k] = a[k];
-          vals[BY + lane + 32 * k] = b[k];
-          vals[2 * BY + lane + 32 * k] = g[k];
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(v_full);
-        if (j + 1 < n_yt) fetch(j + 1);
-      }
     } else if (warp == MMA_WARP) {
       // ------------------------------------------------------------------ MMA issuer
       if (lane == 0) {
@@ -261,8 +220,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int r = wq * 32 + lane;
     const int xidx = x0 + r;
     const float c = p.c;
-    float nAr = 0.f, nBr = 0.f, Gr = 0.f;  // dQ kernel: the row's folded values
-    if (!KSTAT && xidx < p.NQ) {
+    float nAr = 0.f, nBr = 0.f, Gr = 0.f;  // the row's folded values
+    if (xidx < p.NQ) {
       const size_t o = (size_t)bh * p.NQ + xidx;
       const float l1v = lse1[o], l2v = lse2[o];
       nAr = -l1v * kLog2e;
@@ -278,12 +237,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       __syncwarp();
       if (!ok) break;
       tc_fence_after();
-      const int ylo = (y_first + j) * BY + grp * 32;
-      bool masked;
-      if (KSTAT)  // query columns ylo.., key row xidx
-        masked = (ylo + 31 >= p.NQ) || (xidx >= p.NK) || (p.causal && xidx > ylo + p.off);
-      else  // key columns ylo.., query row xidx
-        masked = (ylo + 31 >= p.NK) || (xidx >= p.NQ) || (p.causal && ylo + 31 > xidx + p.off);
+      const int ylo = j * BY + grp * 32;  // key columns ylo.., query row xidx
+      const bool masked = (ylo + 31 >= p.NK) || (xidx >= p.NQ) || (p.causal && ylo + 31 > xidx + p.off);
       uint32_t pk[16];
       // Two halves of 16 columns: the second half is read after the first is
       // computed, and the logits' TMEM is released once both are in registers.
@@ -299,36 +254,18 @@ __global__ void __launch_bounds__(THREADS, 1)
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(s_free);
-        } else if (KSTAT) {
-          ok = mbar_wait(v_full, j & 1, status, abort_flag);
-          __syncwarp();
-          if (!ok) break;
         }
         const int y = ylo + 16 * h;
-        if (KSTAT) {
-          const float* vh = vals + grp * 32 + 16 * h;
-          if (masked)
-            make_ds_cols<SETTING, true, 16, BY>(a, bb, pk + 8 * h, c, p.scale, vh,
-                                                visible_queries<16>(xidx, y, p.NQ, p.NK, p.off, p.causal));
-          else
-            make_ds_cols<SETTING, false, 16, BY>(a, bb, pk + 8 * h, c, p.scale, vh, 0u);
-        } else {
-          if (masked)
-            make_ds_row<SETTING, true, 16>(a, bb, pk + 8 * h, c, p.scale, nAr, nBr, Gr,
-                                           visible_keys<16>(xidx, y, p.NQ, p.NK, p.off, p.causal));
-          else
-            make_ds_row<SETTING, false, 16>(a, bb, pk + 8 * h, c, p.scale, nAr, nBr, Gr, 0u);
-        }
+        if (masked)
+          make_ds_row<SETTING, true, 16>(a, bb, pk + 8 * h, c, p.scale, nAr, nBr, Gr,
+                                         visible_keys<16>(xidx, y, p.NQ, p.NK, p.off, p.causal));
+        else
+          make_ds_row<SETTING, false, 16>(a, bb, pk + 8 * h, c, p.scale, nAr, nBr, Gr, 0u);
         if (h == 0)  // first half final before the second half is read
           asm volatile("" : "+r"(pk[0]), "+r"(pk[1]), "+r"(pk[2]), "+r"(pk[3]), "+r"(pk[4]), "+r"(pk[5]),
                        "+r"(pk[6]), "+r"(pk[7])::"memory");
       }
-      if (!ok) break;
       reg_fence16(pk);
-      if (KSTAT) {
-        __syncwarp();
-        if (lane == 0) mbar_arrive(v_free);
-      }
       // dS buffer b is free once the gradient MMA of tile j - 2 is done
       if (j >= 2) {
         ok = mbar_wait(ds_free + 8 * b, ((j >> 1) - 1) & 1, status, abort_flag);
@@ -374,26 +311,349 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
+// ---------------------------------------------------------------------------
+// The dK kernel.  A block owns 128 keys (K1, K2 stationary in smem) and streams
+// 128-query tiles, but computes the logits with the query tile as the MMA's M
+// operand, so the 128 TMEM lanes are queries: a dS thread owns a query row and
+// holds its folded values in registers (no shared-memory loads in the dS loop).
+// dS goes to smem as dS[query][key] and dK += dS^T Q_opt reads it MN-major, so
+// the dK accumulator has the keys on its lanes.
+//   S_a = Q_a K_a^T, S_b = Q_b K_b^T   SS, K-major, TMEM [0, 128) and [128, 256) (lanes = queries)
+//   dK += dS^T Q_opt                   SS: A = dS read MN-major (M = keys), B = Q_opt MN-major -> [256, 256 + D)
+//   warps 0-15  dS warps: thread = query row, group g = key columns [32g, 32g + 32);
+//               at the end, thread = key row, group g = d columns [32g, 32g + 32) of dK
+//   warp 16     TMA producer: K1, K2 once, then the other Q tile through two slots
+//   warp 17     TMEM owner and MMA issuer
+//   warp 18     TMA producer of Q_opt (two slots, held until the dK MMA)
+namespace dkk {
+constexpr int BK = 128, BQ = 128, SLOTS = 2;
+constexpr uint32_t kColSA = 0, kColSB = 128, kColG = 256;
+
+template <int D>
+struct Smem {
+  static constexpr int TK = BK * D * 2, TQ = BQ * D * 2;
+  static constexpr int OFF_KA = 0;                       // the other K (K1 in setting 1, K2 in setting 2)
+  static constexpr int OFF_KB = TK;                      // K_opt
+  static constexpr int OFF_QO = 2 * TK;                  // Q_opt slots
+  static constexpr int OFF_QT = OFF_QO + SLOTS * TQ;     // the other Q tile's slots
+  static constexpr int OFF_DS = OFF_QT + SLOTS * TQ;     // dS[query][key] bf16: 2 halves of [128 queries][128 B]
+  static constexpr int OFF_BAR = OFF_DS + BQ * BK * 2;
+  // k_full, qo_full[2], qo_empty[2], qt_full[2], qt_empty[2], sa_full, sa_free, sb_full, sb_free,
+  // ds_full, ds_free, g_done; then the TMEM base address slot and the abort flag
+  static constexpr int BAR_SLOT = 16 * 8;
+  static constexpr int BYTES = OFF_BAR + BAR_SLOT + 16 + 1024;
+};
+static_assert(Smem<128>::BYTES <= 227 * 1024, "shared memory");
+}  // namespace dkk
+
+template <int D, int SETTING>
+__global__ void __launch_bounds__(THREADS, 1)
+    bwd_dk_kernel(const Problem p, const float* __restrict__ lse1, const float* __restrict__ lse2,
+                  const float* __restrict__ klv, const float* __restrict__ gv, __nv_bfloat16* __restrict__ dk_out,
+                  int* status, const __grid_constant__ CUtensorMap mk1, const __grid_constant__ CUtensorMap mk2,
+                  const __grid_constant__ CUtensorMap mq1, const __grid_constant__ CUtensorMap mq2) {
+  using dkk::BK;
+  using dkk::BQ;
+  using dkk::SLOTS;
+  using L = dkk::Smem<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  const uint32_t sb = smem_u32(smem);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int bh = blockIdx.x % p.BH;
+  const int kt = (int)(blockIdx.x / p.BH);  // longest first: the first key tiles see the most queries
+  const int k0 = kt * BK;
+  const int q_begin = p.causal ? max(0, k0 - p.off) / BQ * BQ : 0;
+  const int n_qt = (p.NQ - q_begin + BQ - 1) / BQ;
+
+  const uint32_t bar = sb + L::OFF_BAR;
+  const uint32_t k_full = bar, qo_full = bar + 8, qo_empty = bar + 24, qt_full = bar + 40, qt_empty = bar + 56,
+                 sa_full = bar + 72, sa_free = bar + 80, sb_full = bar + 88, sb_free = bar + 96, ds_full = bar + 104,
+                 ds_free = bar + 112, g_done = bar + 120, slot = bar + L::BAR_SLOT;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_BAR + L::BAR_SLOT + 4);
+
+  if (threadIdx.x == 0) {
+    mbar_init(k_full, 1);
+    for (int s = 0; s < SLOTS; ++s) {
+      mbar_init(qo_full + 8 * s, 1);
+      mbar_init(qo_empty + 8 * s, 1);
+      mbar_init(qt_full + 8 * s, 1);
+      mbar_init(qt_empty + 8 * s, 1);
+    }
+    mbar_init(sa_full, 1);
+    mbar_init(sa_free, DS_WARPS);
+    mbar_init(sb_full, 1);
+    mbar_init(sb_free, DS_WARPS);
+    mbar_init(ds_full, DS_WARPS);
+    mbar_init(ds_free, 1);
+    mbar_init(g_done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == MMA_WARP) {
+    tmem_alloc(slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::OFF_BAR + L::BAR_SLOT);
+
+  if (warp >= DS_WARPS) {
+    setmaxnreg_dec_other();
+    if (warp == PRODUCER_WARP) {
+      // ------------------------------------------------------------------ TMA producer
+      if (lane == 0) {
+        mbar_arrive_expect_tx(k_full, 2 * L::TK);
+#pragma unroll
+        for (int h = 0; h < D / 64; ++h) {
+          tma_load_3d(sb + L::OFF_KA + h * BK * 128, SETTING == 1 ? &mk1 : &mk2, k_full, h * 64, k0, bh);
+          tma_load_3d(sb + L::OFF_KB + h * BK * 128, SETTING == 1 ? &mk2 : &mk1, k_full, h * 64, k0, bh);
+        }
+        const CUtensorMap* mqa = SETTING == 1 ? &mq1 : &mq2;
+        int issued = 0;
+        for (int j = 0; j < n_qt; ++j) {
+          const int s = j % SLOTS;
+          if (j >= SLOTS && !mbar_wait(qt_empty + 8 * s, ((j / SLOTS) - 1) & 1, status, abort_flag)) break;
+          mbar_arrive_expect_tx(qt_full + 8 * s, L::TQ);
+#pragma unroll
+          for (int h = 0; h < D / 64; ++h)
+            tma_load_3d(sb + L::OFF_QT + s * L::TQ + h * BQ * 128, mqa, qt_full + 8 * s, h * 64, q_begin + j * BQ,
+                        bh);
+          issued = j + 1;
+        }
+        mbar_drain(k_full, 0, status);
+        for (int j = max(0, issued - SLOTS); j < issued; ++j)
+          mbar_drain(qt_full + 8 * (j % SLOTS), (j / SLOTS) & 1, status);
+      }
+      __syncwarp();
+    } else if (warp == QOPT_WARP) {
+      // ------------------------------------------------------------------ TMA producer of Q_opt
+      if (lane == 0) {
+        const CUtensorMap* mqb = SETTING == 1 ? &mq2 : &mq1;
+        int issued = 0;
+        for (int j = 0; j < n_qt; ++j) {
+          const int s = j % SLOTS;
+          if (j >= SLOTS && !mbar_wait(qo_empty + 8 * s, ((j / SLOTS) - 1) & 1, status, abort_flag)) break;
+          mbar_arrive_expect_tx(qo_full + 8 * s, L::TQ);
+#pragma unroll
+          for (int h = 0; h < D / 64; ++h)
+            tma_load_3d(sb + L::OFF_QO + s * L::TQ + h * BQ * 128, mqb, qo_full + 8 * s, h * 64, q_begin + j * BQ,
+                        bh);
+          issued = j + 1;
+        }
+        for (int j = max(0, issued - SLOTS); j < issued; ++j)
+          mbar_drain(qo_full + 8 * (j % SLOTS), (j / SLOTS) & 1, status);
+      }
+      __syncwarp();
+    } else if (warp == MMA_WARP) {
+      // ------------------------------------------------------------------ MMA issuer
+      if (lane == 0) {
+        constexpr uint32_t id_s = idesc_bf16(BQ, BK, false, false);
+        constexpr uint32_t id_g = idesc_bf16(BK, D, true, true);
+        const uint64_t kad = sdesc_sw128(sb + L::OFF_KA, 0, 1024), kbd = sdesc_sw128(sb + L::OFF_KB, 0, 1024);
+        const uint64_t dsm = sdesc_sw128(sb + L::OFF_DS, BQ * 128, 1024);  // dS^T: M = keys, MN-major
+        bool ok = mbar_wait(k_full, 0, status, abort_flag);
+        for (int j = 0; ok && j <= n_qt; ++j) {
+          if (j < n_qt) {
+            const int s = j % SLOTS;
+            if (!mbar_wait(qt_full + 8 * s, (j / SLOTS) & 1, status, abort_flag)) break;
+            if (j >= 1 && !mbar_wait(sa_free, (j - 1) & 1, status, abort_flag)) break;
+            tc_fence_after();
+            const uint64_t qad = sdesc_sw128(sb + L::OFF_QT + s * L::TQ, 0, 1024);
+#pragma unroll
+            for (int ks = 0; ks < D / 16; ++ks) {
+              const uint32_t off = (ks >> 2) * (128 * 128) + (ks & 3) * 32;  // BQ == BK: same half stride
+              mma_ss(tmem + dkk::kColSA, sdesc_add(qad, off), sdesc_add(kad, off), id_s, ks > 0);
+            }
+            mma_commit(sa_full);
+            mma_commit(qt_empty + 8 * s);  // the other Q tile is read only by S_a
+            if (!mbar_wait(qo_full + 8 * s, (j / SLOTS) & 1, status, abort_flag)) break;
+            if (j >= 1 && !mbar_wait(sb_free, (j - 1) & 1, status, abort_flag)) break;
+            tc_fence_after();
+            const uint64_t qbd = sdesc_sw128(sb + L::OFF_QO + s * L::TQ, 0, 1024);
+#pragma unroll
+            for (int ks = 0; ks < D / 16; ++ks) {
+              const uint32_t off = (ks >> 2) * (128 * 128) + (ks & 3) * 32;
+              mma_ss(tmem + dkk::kColSB, sdesc_add(qbd, off), sdesc_add(kbd, off), id_s, ks > 0);
+            }
+            mma_commit(sb_full);
+          }
+          if (j >= 1) {
+            const int jj = j - 1, s = jj % SLOTS;
+            if (!mbar_wait(ds_full, jj & 1, status, abort_flag)) break;
+            tc_fence_after();
+            // dK += dS^T Q_opt: A = dS[query][key] read MN-major (M = keys), B = Q_opt read MN-major
+            const uint64_t qod = sdesc_sw128(sb + L::OFF_QO + s * L::TQ, BQ * 128, 1024);
+#pragma unroll
+            for (int ks = 0; ks < BQ / 16; ++ks)
+              mma_ss(tmem + dkk::kColG, sdesc_add(dsm, ks * 2048), sdesc_add(qod, ks * 2048), id_g, jj > 0 || ks > 0);
+            mma_commit(qo_empty + 8 * s);
+            mma_commit(ds_free);
+          }
+        }
+        mma_commit(g_done);
+        mbar_drain(g_done, 0, status);
+      }
+      __syncwarp();
+    }
+  } else {
+    setmaxnreg_inc_ds();
+    // ------------------------------------------------------------------ dS warps
+    const int grp = warp >> 2, wq = warp & 3;
+    const int r = wq * 32 + lane;
+    const float c = p.c;
+    const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
+    const uint32_t tcol = tmem + lane_base + grp * 32;
+    const uint32_t dsb = sb + L::OFF_DS;
+    // this row's folded values for query tile j (loaded one tile ahead)
+    auto fetch = [&](int j, float& a, float& b, float& g) {
+      const int q = q_begin + j * BQ + r;
+      a = b = g = 0.f;
+      if (j < n_qt && q < p.NQ) {
+        const size_t o = (size_t)bh * p.NQ + q;
+        const float l1v = lse1[o], l2v = lse2[o];
+        a = -l1v * kLog2e;
+        b = SETTING == 1 ? -l2v * kLog2e : -(l1v - l2v + klv[o]);
+        g = gv[o];
+      }
+    };
+    float nAr, nBr, Gr, nA2, nB2, G2;
+    fetch(0, nAr, nBr, Gr);
+    bool ok = true;
+    for (int j = 0; j < n_qt; ++j) {
+      fetch(j + 1, nA2, nB2, G2);
+      const int q = q_begin + j * BQ + r;
+      ok = mbar_wait(sa_full, j & 1, status, abort_flag);
+      __syncwarp();
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t held[32];  // this thread's 32 columns of S_a
+      tmem_ld32(tcol + dkk::kColSA, held);
+      tmem_ld_wait();
+      reg_fence32(held);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(sa_free);
+      const int kg = k0 + grp * 32;
+      const bool masked = (kg + 31 >= p.NK) || (q >= p.NQ) || (p.causal && kg + 31 > q + p.off);
+      uint32_t pk[16];
+      ok = mbar_wait(sb_full, j & 1, status, abort_flag);
+      __syncwarp();
+      if (!ok) break;
+      tc_fence_after();
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t half[16];
+        tmem_ld16(tcol + dkk::kColSB + 16 * h, half);
+        tmem_ld_wait();
+        reg_fence16(half);
+        if (h == 1) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(sb_free);
+        }
+        const uint32_t(&ha)[16] = *reinterpret_cast<const uint32_t(*)[16]>(&held[16 * h]);
+        auto run = [&](const uint32_t(&s1)[16], const uint32_t(&s2)[16]) {
+          if (masked)
+            make_ds_row<SETTING, true, 16>(s1, s2, pk + 8 * h, c, p.scale, nAr, nBr, Gr,
+                                           visible_keys<16>(q, kg + 16 * h, p.NQ, p.NK, p.off, p.causal));
+          else
+            make_ds_row<SETTING, false, 16>(s1, s2, pk + 8 * h, c, p.scale, nAr, nBr, Gr, 0u);
+        };
+        if (SETTING == 1)
+          run(ha, half);  // S_a = S1, S_b = S2
+        else
+          run(half, ha);  // S_a = S2, S_b = S1
+        if (h == 0)  // first half final before the second half is read
+          asm volatile("" : "+r"(pk[0]), "+r"(pk[1]), "+r"(pk[2]), "+r"(pk[3]), "+r"(pk[4]), "+r"(pk[5]),
+                       "+r"(pk[6]), "+r"(pk[7])::"memory");
+      }
+      reg_fence16(pk);
+      // dS smem is free once the dK MMA of the previous tile is done
+      if (j >= 1) {
+        ok = mbar_wait(ds_free, (j - 1) & 1, status, abort_flag);
+        __syncwarp();
+        if (!ok) break;
+      }
+#pragma unroll
+      for (int cch = 0; cch < 4; ++cch) {
+        const uint32_t dst = sw128<BQ>(dsb, r, grp * 4 + cch);
+        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(pk[4 * cch]), "r"(pk[4 * cch + 1]),
+                     "r"(pk[4 * cch + 2]), "r"(pk[4 * cch + 3])
+                     : "memory");
+      }
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(ds_full);
+      nAr = nA2;
+      nBr = nB2;
+      Gr = G2;
+    }
+    // ---- dK out: thread = key row k0 + r, group g writes d columns [32g, 32g + 32)
+    const bool got = ok && mbar_wait(g_done, 0, status, abort_flag);
+    __syncwarp();
+    const int key = k0 + r;
+    if (got && grp * 32 < D) {
+      tc_fence_after();
+      uint32_t g0[32];
+      tmem_ld32(tmem + lane_base + dkk::kColG + grp * 32, g0);
+      tmem_ld_wait();
+      reg_fence32(g0);
+      if (key < p.NK) {
+        __nv_bfloat16* dst = dk_out + ((size_t)bh * p.NK + key) * D + grp * 32;
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          const uint32_t* src = &g0[v * 8];
+          uint4 o;
+          o.x = pack_bf16(__uint_as_float(src[0]) * p.scale, __uint_as_float(src[1]) * p.scale);
+          o.y = pack_bf16(__uint_as_float(src[2]) * p.scale, __uint_as_float(src[3]) * p.scale);
+          o.z = pack_bf16(__uint_as_float(src[4]) * p.scale, __uint_as_float(src[5]) * p.scale);
+          o.w = pack_bf16(__uint_as_float(src[6]) * p.scale, __uint_as_float(src[7]) * p.scale);
+          reinterpret_cast<uint4*>(dst)[v] = o;
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == MMA_WARP) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
 constexpr int kOneBlockPerSmSmem = 120 * 1024;  // a block owns all 512 TMEM columns
 
-template <int D, int SETTING, bool KSTAT>
-cudaError_t launch_one(const Problem& p, const BwdIn& in, void* out, int* status, cudaStream_t st) {
-  const void* x1 = KSTAT ? in.k1 : in.q1;
-  const void* x2 = KSTAT ? in.k2 : in.q2;
-  const void* y1 = KSTAT ? in.q1 : in.k1;
-  const void* y2 = KSTAT ? in.q2 : in.k2;
-  const int NX = KSTAT ? p.NK : p.NQ, NY = KSTAT ? p.NQ : p.NK;
+template <int D, int SETTING>
+cudaError_t launch_dq(const Problem& p, const BwdIn& in, void* dq, int* status, cudaStream_t st) {
   CUtensorMap mx1, mx2, my1, my2;
-  if (!encode_tile_map(&mx1, x1, D, NX, p.BH, BX) || !encode_tile_map(&mx2, x2, D, NX, p.BH, BX) ||
-      !encode_tile_map(&my1, y1, D, NY, p.BH, BY) || !encode_tile_map(&my2, y2, D, NY, p.BH, BY))
+  if (!encode_tile_map(&mx1, in.q1, D, p.NQ, p.BH, BX) || !encode_tile_map(&mx2, in.q2, D, p.NQ, p.BH, BX) ||
+      !encode_tile_map(&my1, in.k1, D, p.NK, p.BH, BY) || !encode_tile_map(&my2, in.k2, D, p.NK, p.BH, BY))
     return cudaErrorInvalidValue;
   const int smem = Smem<D>::BYTES > kOneBlockPerSmSmem ? Smem<D>::BYTES : kOneBlockPerSmSmem;
-  auto kern = bwd_tc_kernel<D, SETTING, KSTAT>;
+  auto kern = bwd_dq_kernel<D, SETTING>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  const long long blocks = (long long)p.BH * ((NX + BX - 1) / BX);
-  kern<<<(unsigned)blocks, THREADS, smem, st>>>(p, in.lse1, in.lse2, in.kl, in.g, static_cast<__nv_bfloat16*>(out),
+  const long long blocks = (long long)p.BH * ((p.NQ + BX - 1) / BX);
+  kern<<<(unsigned)blocks, THREADS, smem, st>>>(p, in.lse1, in.lse2, in.kl, in.g, static_cast<__nv_bfloat16*>(dq),
                                                 status, mx1, mx2, my1, my2);
+  return cudaGetLastError();
+}
+
+template <int D, int SETTING>
+cudaError_t launch_dk(const Problem& p, const BwdIn& in, void* dk, int* status, cudaStream_t st) {
+  CUtensorMap mk1, mk2, mq1, mq2;
+  if (!encode_tile_map(&mk1, in.k1, D, p.NK, p.BH, dkk::BK) || !encode_tile_map(&mk2, in.k2, D, p.NK, p.BH, dkk::BK) ||
+      !encode_tile_map(&mq1, in.q1, D, p.NQ, p.BH, dkk::BQ) || !encode_tile_map(&mq2, in.q2, D, p.NQ, p.BH, dkk::BQ))
+    return cudaErrorInvalidValue;
+  const int smem = dkk::Smem<D>::BYTES > kOneBlockPerSmSmem ? dkk::Smem<D>::BYTES : kOneBlockPerSmSmem;
+  auto kern = bwd_dk_kernel<D, SETTING>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  const long long blocks = (long long)p.BH * ((p.NK + dkk::BK - 1) / dkk::BK);
+  kern<<<(unsigned)blocks, THREADS, smem, st>>>(p, in.lse1, in.lse2, in.kl, in.g, static_cast<__nv_bfloat16*>(dk),
+                                                status, mk1, mk2, mq1, mq2);
   return cudaGetLastError();
 }
 
@@ -401,12 +661,11 @@ template <int D>
 cudaError_t separate_d(const Problem& p, int setting, const BwdIn& in, void* dq, void* dk, int* status,
                        cudaStream_t st) {
   if (dq) {
-    cudaError_t e = setting == 1 ? launch_one<D, 1, false>(p, in, dq, status, st)
-                                 : launch_one<D, 2, false>(p, in, dq, status, st);
+    cudaError_t e = setting == 1 ? launch_dq<D, 1>(p, in, dq, status, st) : launch_dq<D, 2>(p, in, dq, status, st);
     if (e != cudaSuccess) return e;
   }
   if (!dk) return cudaSuccess;
-  return setting == 1 ? launch_one<D, 1, true>(p, in, dk, status, st) : launch_one<D, 2, true>(p, in, dk, status, st);
+  return setting == 1 ? launch_dk<D, 1>(p, in, dk, status, st) : launch_dk<D, 2>(p, in, dk, status, st);
 }
 
 }  // namespace

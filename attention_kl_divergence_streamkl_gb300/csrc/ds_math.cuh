@@ -20,16 +20,6 @@
 
 namespace skl {
 
-// Bit k set iff query column q0 + k (k < N <= 16) sees `key`: the key exists,
-// the query exists, and (causal) key <= query + off.
-template <int N>
-__device__ __forceinline__ uint32_t visible_queries(int key, int q0, int nq, int nk, int off, int causal) {
-  if (key >= nk) return 0u;
-  const int lo = causal ? min(max(key - off - q0, 0), N) : 0;
-  const int hi = min(max(nq - q0, 0), N);
-  return hi > lo ? ((1u << hi) - 1u) & ~((1u << lo) - 1u) : 0u;
-}
-
 // Bit k set iff key column k0 + k (k < N <= 16) is seen by query `q`.
 template <int N>
 __device__ __forceinline__ uint32_t visible_keys(int q, int k0, int nq, int nk, int off, int causal) {
@@ -66,30 +56,6 @@ __device__ __forceinline__ uint32_t ds_pair(float2 s1, float2 s2, float2 cc, flo
     ds = fmul2(fmul2(G, p1), ffma2(sc, fsub2(s1, s2), nB));
   }
   return pack_bf16(ds.x, ds.y);
-}
-
-// Thread = one key, N query columns with their folded values in vals[0..N),
-// vals[VSTRIDE..), vals[2 VSTRIDE..) (nA, nB, G); dS packed as bf16 pairs.
-template <int SETTING, bool MASKED, int N, int VSTRIDE>
-__device__ __forceinline__ void make_ds_cols(const uint32_t (&a)[N], const uint32_t (&b)[N], uint32_t* pk, float c,
-                                             float scale, const float* vals, uint32_t visible) {
-  const float2 cc = make_float2(c, c), sc = make_float2(scale, scale);
-#pragma unroll
-  for (int i = 0; i < N; i += 4) {
-    const float4 nA4 = *reinterpret_cast<const float4*>(vals + i);
-    const float4 nB4 = *reinterpret_cast<const float4*>(vals + VSTRIDE + i);
-    const float4 G4 = *reinterpret_cast<const float4*>(vals + 2 * VSTRIDE + i);
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int k = i + 2 * h;
-      const float2 nA = h ? make_float2(nA4.z, nA4.w) : make_float2(nA4.x, nA4.y);
-      const float2 nB = h ? make_float2(nB4.z, nB4.w) : make_float2(nB4.x, nB4.y);
-      const float2 G = h ? make_float2(G4.z, G4.w) : make_float2(G4.x, G4.y);
-      const float2 s1 = make_float2(__uint_as_float(a[k]), __uint_as_float(a[k + 1]));
-      const float2 s2 = make_float2(__uint_as_float(b[k]), __uint_as_float(b[k + 1]));
-      pk[k / 2] = ds_pair<SETTING, MASKED>(s1, s2, cc, sc, nA, nB, G, visible, k);
-    }
-  }
 }
 
 // Thread = one query row with its folded values (nA, nB, G), N key columns.
