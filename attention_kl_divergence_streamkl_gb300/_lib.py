@@ -9,6 +9,12 @@ the library is missing, every call raises.
 Inputs given as CPU tensors are copied to the current CUDA device on the
 current stream (non-blocking from pinned memory) and the results are copied
 back, so a host caller uses the same functions.
+
+Device inputs need not be contiguous: any [B, H, N, D] view whose D is
+contiguous, whose other strides are multiples of 8 elements and whose rows do
+not overlap (a [B, N, H, D] tensor permuted, a slice of a packed QKV tensor) is
+passed as it is, with its strides; the gradients come back with the strides of
+the input they belong to.  Other views are copied to a contiguous tensor first.
 """
 from __future__ import annotations
 
@@ -28,7 +34,10 @@ SPLITK_MAX_NQ = 16
 
 class Shape(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int), ("H", ctypes.c_int), ("NQ", ctypes.c_int), ("NK", ctypes.c_int),
-                ("D", ctypes.c_int), ("scale", ctypes.c_float), ("causal", ctypes.c_int)]
+                ("D", ctypes.c_int), ("scale", ctypes.c_float), ("causal", ctypes.c_int),
+                ("q_stride_b", ctypes.c_longlong), ("q_stride_h", ctypes.c_longlong),
+                ("q_stride_n", ctypes.c_longlong), ("k_stride_b", ctypes.c_longlong),
+                ("k_stride_h", ctypes.c_longlong), ("k_stride_n", ctypes.c_longlong)]
 
 
 class StreamKLError(RuntimeError):
@@ -83,8 +92,57 @@ def _check(status: int, where: str) -> None:
         raise StreamKLError(status, where)
 
 
-def make_shape(B, H, NQ, NK, D, scale=None, causal=False) -> Shape:
-    return Shape(int(B), int(H), int(NQ), int(NK), int(D), float(scale or 0.0), int(bool(causal)))
+def make_shape(B, H, NQ, NK, D, scale=None, causal=False, q_strides=(0, 0, 0), k_strides=(0, 0, 0)) -> Shape:
+    """The C shape; q_strides / k_strides are element strides along (b, h, n), zeros = contiguous."""
+    return Shape(int(B), int(H), int(NQ), int(NK), int(D), float(scale or 0.0), int(bool(causal)),
+                 *(int(x) for x in q_strides), *(int(x) for x in k_strides))
+
+
+def _bhn_strides(t: torch.Tensor):
+    """(b, h, n) element strides under which the library can read `t` in place, else None.
+
+    D must be contiguous, the start 16-byte aligned, each stride of an extent > 1
+    a positive multiple of 8 elements and the rows pairwise disjoint (sorted by
+    stride, each stride covers the extent below it).  The stride of an extent-1
+    dimension is never used to address anything; it is replaced by a valid one.
+    """
+    B, H, N, D = t.shape
+    if t.numel() == 0:  # nothing is read; any valid strides do
+        return max(H, 1) * max(N, 1) * D, max(N, 1) * D, D
+    if t.stride(3) != 1 or t.data_ptr() % 16:
+        return None
+    dims = [(t.stride(i), t.size(i)) for i in range(4) if t.size(i) > 1]
+    if any(st <= 0 for st, _ in dims):
+        return None
+    span = 0
+    for st, n in sorted(dims):
+        if st < span:
+            return None
+        span = st * n
+    sn = t.stride(2) if t.size(2) > 1 else D
+    sh = t.stride(1) if t.size(1) > 1 else 8
+    sb = t.stride(0) if t.size(0) > 1 else 8
+    if sn < D or any(x % 8 for x in (sb, sh, sn)):
+        return None
+    return sb, sh, sn
+
+
+def _pair(a: torch.Tensor, b: torch.Tensor):
+    """The two tensors of a pair (Q1/Q2 or K1/K2) and their shared (b, h, n) strides."""
+    sa, sb = _bhn_strides(a), _bhn_strides(b)
+    if sa is None or sa != sb:
+        a, b = a.contiguous(), b.contiguous()
+        sa = _bhn_strides(a)
+        if sa is None:
+            raise ValueError("inputs must be 16-byte aligned")
+    return a, b, sa
+
+
+def _grad_like(t: torch.Tensor, strides, rows) -> torch.Tensor:
+    """A bf16 output with the (b, h, n) strides the library writes `t`'s gradient with."""
+    B, H, _, D = t.shape
+    return torch.empty_strided((B, H, rows, D), (strides[0], strides[1], strides[2], 1), dtype=torch.bfloat16,
+                               device=t.device)
 
 
 def _ptr(t: Optional[torch.Tensor]):
@@ -96,7 +154,7 @@ def _stream(device: torch.device):
 
 
 def _prep(q1, k1, q2, k2):
-    """Validates the four inputs; returns (device tensors, shape, was_host)."""
+    """Validates the four inputs; returns (device tensors, was_host, q strides, k strides)."""
     ts = [q1, k1, q2, k2]
     for t in ts:
         if t.dtype != torch.bfloat16:
@@ -110,11 +168,11 @@ def _prep(q1, k1, q2, k2):
     if host:
         dev = torch.device("cuda", torch.cuda.current_device())
         ts = [t.contiguous().to(dev, non_blocking=True) for t in ts]
-    else:
-        ts = [t.contiguous() for t in ts]
-        if any(t.device != ts[0].device for t in ts):
-            raise ValueError("inputs on different devices")
-    return ts, host
+    elif any(t.device != ts[0].device for t in ts):
+        raise ValueError("inputs on different devices")
+    q1, q2, qs = _pair(ts[0], ts[2])
+    k1, k2, ks = _pair(ts[1], ts[3])
+    return [q1, k1, q2, k2], host, qs, ks
 
 
 def _rows(t: Optional[torch.Tensor], dev, shape3, name):
@@ -135,9 +193,9 @@ def _back(ts, host):
 
 def fwd(q1, k1, q2, k2, scale=None, causal=False):
     """KL, LSE1, LSE2 fp32 [B, H, N_Q] (one-pass forward)."""
-    (q1, k1, q2, k2), host = _prep(q1, k1, q2, k2)
+    (q1, k1, q2, k2), host, qs, ks = _prep(q1, k1, q2, k2)
     B, H, NQ, D = q1.shape
-    s = make_shape(B, H, NQ, k1.shape[2], D, scale, causal)
+    s = make_shape(B, H, NQ, k1.shape[2], D, scale, causal, qs, ks)
     kl, l1, l2 = (torch.empty((B, H, NQ), dtype=torch.float32, device=q1.device) for _ in range(3))
     _check(lib().streamkl_fwd(_ptr(q1), _ptr(k1), _ptr(q2), _ptr(k2), s, _ptr(kl), _ptr(l1), _ptr(l2),
                               _stream(q1.device)), "streamkl_fwd")
@@ -153,9 +211,9 @@ def splitk_plan(B, H, NQ, NK, D, num_sms=0, causal=False) -> int:
 
 def fwd_splitk(q1, k1, q2, k2, scale=None, causal=False, num_splits=0):
     """Split-K forward for N_Q <= 16: KL, LSE1, LSE2 fp32 [B, H, N_Q]."""
-    (q1, k1, q2, k2), host = _prep(q1, k1, q2, k2)
+    (q1, k1, q2, k2), host, qs, ks = _prep(q1, k1, q2, k2)
     B, H, NQ, D = q1.shape
-    s = make_shape(B, H, NQ, k1.shape[2], D, scale, causal)
+    s = make_shape(B, H, NQ, k1.shape[2], D, scale, causal, qs, ks)
     nbytes = ctypes.c_size_t(0)
     _check(lib().streamkl_fwd_splitk_workspace(s, int(num_splits), ctypes.byref(nbytes)),
            "streamkl_fwd_splitk_workspace")
@@ -179,11 +237,11 @@ def bwd_workspace_bytes(B, H, NQ, NK, D, bwd_mode=BWD_AUTO, causal=False) -> int
 
 
 def _bwd(setting, q1, k1, q2, k2, lse1, lse2, kl, g, scale, causal, bwd_mode):
-    (q1, k1, q2, k2), host = _prep(q1, k1, q2, k2)
+    (q1, k1, q2, k2), host, qs, ks = _prep(q1, k1, q2, k2)
     B, H, NQ, D = q1.shape
     NK = k1.shape[2]
     dev = q1.device
-    s = make_shape(B, H, NQ, NK, D, scale, causal)
+    s = make_shape(B, H, NQ, NK, D, scale, causal, qs, ks)
     lse1 = _rows(lse1, dev, (B, H, NQ), "lse1")
     lse2 = _rows(lse2, dev, (B, H, NQ), "lse2")
     g = _rows(g, dev, (B, H, NQ), "g")
@@ -191,8 +249,8 @@ def _bwd(setting, q1, k1, q2, k2, lse1, lse2, kl, g, scale, causal, bwd_mode):
     nbytes = ctypes.c_size_t(0)
     _check(lib().streamkl_bwd_workspace(s, int(bwd_mode), ctypes.byref(nbytes)), "streamkl_bwd_workspace")
     ws = torch.empty(max(16, nbytes.value), dtype=torch.uint8, device=dev)
-    dq = torch.empty((B, H, NQ, D), dtype=torch.bfloat16, device=dev) if bwd_mode != BWD_DK_ONLY else None
-    dk = torch.empty((B, H, NK, D), dtype=torch.bfloat16, device=dev) if bwd_mode != BWD_DQ_ONLY else None
+    dq = _grad_like(q1, qs, NQ) if bwd_mode != BWD_DK_ONLY else None
+    dk = _grad_like(k1, ks, NK) if bwd_mode != BWD_DQ_ONLY else None
     if setting == 1:
         st = lib().streamkl_bwd_s1(_ptr(q1), _ptr(k1), _ptr(q2), _ptr(k2), s, _ptr(lse1), _ptr(lse2), _ptr(g),
                                    _ptr(dq), _ptr(dk), int(bwd_mode), _ptr(ws), nbytes.value, _stream(dev))

@@ -38,6 +38,26 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 constexpr long long kMaxGridY = 65535;
 constexpr int kMaxRows = 1 << 30;
 
+// Element strides of a [B, H, N, D] view: all zero selects the contiguous
+// layout; otherwise each is positive and a multiple of 8 elements (16 bytes, the
+// TMA stride granule), and a row holds at least D elements.
+bool strides_ok(long long sb, long long sh, long long sn, int H, int N, int D, long long* ob, long long* oh,
+                long long* on) {
+  if (sb == 0 && sh == 0 && sn == 0) {
+    *on = D;
+    *oh = (long long)N * D;
+    *ob = (long long)H * N * D;
+    return true;
+  }
+  if (sb <= 0 || sh <= 0 || sn < D) return false;
+  if (sb % 8 || sh % 8 || sn % 8) return false;
+  if (sb >= (1ll << 38) || sh >= (1ll << 38) || sn >= (1ll << 38)) return false;  // TMA strides below 2^40 bytes
+  *ob = sb;
+  *oh = sh;
+  *on = sn;
+  return true;
+}
+
 streamkl_status validate(const streamkl_shape& s, Problem* p) {
   if (s.B <= 0 || s.H <= 0 || s.NQ < 0 || s.NK <= 0 || s.D <= 0) return STREAMKL_ERR_INVALID;
   if (!(s.scale == s.scale) || isinf(s.scale)) return STREAMKL_ERR_INVALID;
@@ -56,6 +76,9 @@ streamkl_status validate(const streamkl_shape& s, Problem* p) {
   p->off = s.NK - s.NQ;
   p->scale = s.scale > 0.f ? s.scale : 1.0f / sqrtf((float)s.D);
   p->c = p->scale * kLog2e;
+  if (!strides_ok(s.q_stride_b, s.q_stride_h, s.q_stride_n, s.H, s.NQ, s.D, &p->qs_b, &p->qs_h, &p->qs_n) ||
+      !strides_ok(s.k_stride_b, s.k_stride_h, s.k_stride_n, s.H, s.NK, s.D, &p->ks_b, &p->ks_h, &p->ks_n))
+    return STREAMKL_ERR_INVALID;
   return STREAMKL_OK;
 }
 
@@ -121,14 +144,15 @@ __global__ void wait_timeout_probe_kernel(unsigned long long limit_ns, int* stat
 
 }  // namespace
 
-bool encode_tile_map(CUtensorMap* map, const void* base, int D, int N, int BH, int box_rows) {
+bool encode_tile_map(CUtensorMap* map, const void* base, int D, int N, int H, int B, long long sn, long long sh,
+                     long long sb, int box_rows) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
-  const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)N, (cuuint64_t)BH};
-  const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)N * D * 2};
-  const cuuint32_t box[3] = {64u, (cuuint32_t)box_rows, 1u};
-  const cuuint32_t estr[3] = {1u, 1u, 1u};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+  const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)N, (cuuint64_t)H, (cuuint64_t)B};
+  const cuuint64_t strides[3] = {(cuuint64_t)sn * 2, (cuuint64_t)sh * 2, (cuuint64_t)sb * 2};
+  const cuuint32_t box[4] = {64u, (cuuint32_t)box_rows, 1u, 1u};
+  const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }

@@ -105,6 +105,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int n_qt = (p.NQ + BQ - 1) / BQ;
   const int bh = (int)(blockIdx.x / n_qt);               // heads in order (their dk_acc rows stay in L2), ...
   const int qt = n_qt - 1 - (int)(blockIdx.x % n_qt);    // ... and within a head the longest (last) query tiles first
+  const int mh = bh % p.H, mb = bh / p.H;  // head and batch coordinates of the tensor maps
   const int q0 = qt * BQ;
   const int q_last = min(p.NQ, q0 + BQ) - 1;
   const int kend = p.causal ? min(p.NK, q_last + p.off + 1) : p.NK;
@@ -159,8 +160,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         mbar_arrive_expect_tx(q_full, 2 * L::TQ);
 #pragma unroll
         for (int h = 0; h < D / 64; ++h) {
-          tma_load_3d(sb + L::OFF_Q1 + h * BQ * 128, &mq1, q_full, h * 64, q0, bh);
-          tma_load_3d(sb + L::OFF_Q2 + h * BQ * 128, &mq2, q_full, h * 64, q0, bh);
+          tma_load_4d(sb + L::OFF_Q1 + h * BQ * 128, &mq1, q_full, h * 64, q0, mh, mb);
+          tma_load_4d(sb + L::OFF_Q2 + h * BQ * 128, &mq2, q_full, h * 64, q0, mh, mb);
         }
         const CUtensorMap* mka = SETTING == 1 ? &mk1 : &mk2;
         int issued = 0;
@@ -170,7 +171,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           mbar_arrive_expect_tx(kt_full + 8 * s, L::TK);
 #pragma unroll
           for (int h = 0; h < D / 64; ++h)
-            tma_load_3d(sb + L::OFF_KT + s * L::TK + h * BK * 128, mka, kt_full + 8 * s, h * 64, j * BK, bh);
+            tma_load_4d(sb + L::OFF_KT + s * L::TK + h * BK * 128, mka, kt_full + 8 * s, h * 64, j * BK, mh, mb);
           issued = j + 1;
         }
         mbar_drain(q_full, 0, status);
@@ -191,7 +192,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           mbar_arrive_expect_tx(ko_full + 8 * s, L::TK);
 #pragma unroll
           for (int h = 0; h < D / 64; ++h)
-            tma_load_3d(sb + L::OFF_KO + s * L::TK + h * BK * 128, mkb, ko_full + 8 * s, h * 64, j * BK, bh);
+            tma_load_4d(sb + L::OFF_KO + s * L::TK + h * BK * 128, mkb, ko_full + 8 * s, h * 64, j * BK, mh, mb);
           issued = j + 1;
         }
         for (int j = max(0, issued - SLOTS); j < issued; ++j)
@@ -386,7 +387,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       tmem_ld_wait();
       reg_fence32(g0);
       if (row < p.NQ) {
-        __nv_bfloat16* dst = dq_out + ((size_t)bh * p.NQ + row) * D + grp * 32;
+        __nv_bfloat16* dst = dq_out + row_offset(bh, p.H, row, p.qs_b, p.qs_h, p.qs_n) + grp * 32;
 #pragma unroll
         for (int v = 0; v < 4; ++v) {
           const uint32_t* src = &g0[v * 8];
@@ -413,8 +414,8 @@ constexpr int kOneBlockPerSmSmem = 120 * 1024;  // a block owns all 512 TMEM col
 template <int D, int SETTING>
 cudaError_t launch_fused(const Problem& p, const BwdIn& in, void* dq, float* dk_acc, int* status, cudaStream_t st) {
   CUtensorMap mq1, mq2, mk1, mk2;
-  if (!encode_tile_map(&mq1, in.q1, D, p.NQ, p.BH, BQ) || !encode_tile_map(&mq2, in.q2, D, p.NQ, p.BH, BQ) ||
-      !encode_tile_map(&mk1, in.k1, D, p.NK, p.BH, BK) || !encode_tile_map(&mk2, in.k2, D, p.NK, p.BH, BK))
+  if (!encode_q_map(&mq1, in.q1, p, BQ) || !encode_q_map(&mq2, in.q2, p, BQ) ||
+      !encode_k_map(&mk1, in.k1, p, BK) || !encode_k_map(&mk2, in.k2, p, BK))
     return cudaErrorInvalidValue;
   const int smem = Smem<D>::BYTES > kOneBlockPerSmSmem ? Smem<D>::BYTES : kOneBlockPerSmSmem;
   auto kern = bwd_fused_tc_kernel<D, SETTING>;
@@ -427,16 +428,22 @@ cudaError_t launch_fused(const Problem& p, const BwdIn& in, void* dq, float* dk_
 }
 
 // dK (bf16) = scale * dK accumulator (fp32); 8 elements per thread.
-__global__ void __launch_bounds__(256) acc_convert_kernel(const float4* __restrict__ acc, uint4* __restrict__ out,
-                                                          size_t n8, float scale) {
+// dK = scale * acc, rounded to bf16 and written with dK's own strides; acc is
+// the contiguous fp32 [B*H, N_K, D] accumulator.  One thread converts 8 values.
+template <int D>
+__global__ void __launch_bounds__(256) acc_convert_kernel(const float4* __restrict__ acc, __nv_bfloat16* __restrict__ out,
+                                                          const Problem p, size_t n8) {
   for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += (size_t)gridDim.x * blockDim.x) {
     const float4 a = acc[2 * i], b = acc[2 * i + 1];
     uint4 o;
-    o.x = pack_bf16(a.x * scale, a.y * scale);
-    o.y = pack_bf16(a.z * scale, a.w * scale);
-    o.z = pack_bf16(b.x * scale, b.y * scale);
-    o.w = pack_bf16(b.z * scale, b.w * scale);
-    out[i] = o;
+    o.x = pack_bf16(a.x * p.scale, a.y * p.scale);
+    o.y = pack_bf16(a.z * p.scale, a.w * p.scale);
+    o.z = pack_bf16(b.x * p.scale, b.y * p.scale);
+    o.w = pack_bf16(b.z * p.scale, b.w * p.scale);
+    const size_t row = i / (D / 8);
+    const int d = (int)(i % (D / 8)) * 8;
+    const int bh = (int)(row / (size_t)p.NK), key = (int)(row % (size_t)p.NK);
+    *reinterpret_cast<uint4*>(out + row_offset(bh, p.H, key, p.ks_b, p.ks_h, p.ks_n) + d) = o;
   }
 }
 
@@ -451,8 +458,8 @@ cudaError_t fused_d(const Problem& p, int setting, const BwdIn& in, void* dq, vo
   if (e != cudaSuccess) return e;
   const size_t n8 = n / 8;
   const int blocks = (int)((n8 + 255) / 256 < 4096 ? (n8 + 255) / 256 : 4096);
-  acc_convert_kernel<<<blocks > 0 ? blocks : 1, 256, 0, st>>>(reinterpret_cast<const float4*>(dk_acc),
-                                                              static_cast<uint4*>(dk), n8, p.scale);
+  acc_convert_kernel<D><<<blocks > 0 ? blocks : 1, 256, 0, st>>>(reinterpret_cast<const float4*>(dk_acc),
+                                                                 static_cast<__nv_bfloat16*>(dk), p, n8);
   return cudaGetLastError();
 }
 

@@ -86,6 +86,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int NX = p.NQ, NY = p.NK;
   const int n_xt = (NX + BX - 1) / BX;
   const int bh = blockIdx.x % p.BH;
+  const int mh = bh % p.H, mb = bh / p.H;  // head and batch coordinates of the tensor maps
   const int xt = n_xt - 1 - (int)(blockIdx.x / p.BH);  // longest blocks (the last query tiles) first
   const int x0 = xt * BX;
   const int y_end = p.causal ? min(NY, min(NX, x0 + BX) - 1 + p.off + 1) : NY;  // keys the last row sees
@@ -134,8 +135,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         mbar_arrive_expect_tx(x_full, 2 * L::TILE);
 #pragma unroll
         for (int h = 0; h < D / 64; ++h) {
-          tma_load_3d(sb + L::OFF_X1 + h * BX * 128, &mx1, x_full, h * 64, x0, bh);
-          tma_load_3d(sb + L::OFF_X2 + h * BX * 128, &mx2, x_full, h * 64, x0, bh);
+          tma_load_4d(sb + L::OFF_X1 + h * BX * 128, &mx1, x_full, h * 64, x0, mh, mb);
+          tma_load_4d(sb + L::OFF_X2 + h * BX * 128, &mx2, x_full, h * 64, x0, mh, mb);
         }
         // Y_opt is Y2 in setting 1 (Q2 or K2), Y1 in setting 2
         const CUtensorMap* mopt = SETTING == 1 ? &my2 : &my1;
@@ -148,13 +149,13 @@ __global__ void __launch_bounds__(THREADS, 1)
           mbar_arrive_expect_tx(yo_full + 8 * so, L::TILE);
 #pragma unroll
           for (int h = 0; h < D / 64; ++h)
-            tma_load_3d(sb + L::OFF_YO + so * L::TILE + h * BY * 128, mopt, yo_full + 8 * so, h * 64, y0, bh);
+            tma_load_4d(sb + L::OFF_YO + so * L::TILE + h * BY * 128, mopt, yo_full + 8 * so, h * 64, y0, mh, mb);
           issued = j + 1;
           if (j >= YT_SLOTS && !mbar_wait(yt_empty + 8 * st, ((j / YT_SLOTS) - 1) & 1, status, abort_flag)) break;
           mbar_arrive_expect_tx(yt_full + 8 * st, L::TILE);
 #pragma unroll
           for (int h = 0; h < D / 64; ++h)
-            tma_load_3d(sb + L::OFF_YT + st * L::TILE + h * BY * 128, moth, yt_full + 8 * st, h * 64, y0, bh);
+            tma_load_4d(sb + L::OFF_YT + st * L::TILE + h * BY * 128, moth, yt_full + 8 * st, h * 64, y0, mh, mb);
           issued_t = j + 1;
         }
         // copies that may still be landing: the last YO_SLOTS Y_opt tiles and YT_SLOTS other tiles
@@ -289,7 +290,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       tmem_ld_wait();
       reg_fence32(g0);
       if (xidx < NX) {
-        __nv_bfloat16* dst = out + ((size_t)bh * NX + xidx) * D + grp * 32;
+        __nv_bfloat16* dst = out + row_offset(bh, p.H, xidx, p.qs_b, p.qs_h, p.qs_n) + grp * 32;
 #pragma unroll
         for (int v = 0; v < 4; ++v) {
           const uint32_t* src = &g0[v * 8];
@@ -361,6 +362,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t sb = smem_u32(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int bh = blockIdx.x % p.BH;
+  const int mh = bh % p.H, mb = bh / p.H;  // head and batch coordinates of the tensor maps
   const int kt = (int)(blockIdx.x / p.BH);  // longest first: the first key tiles see the most queries
   const int k0 = kt * BK;
   const int q_begin = p.causal ? max(0, k0 - p.off) / BQ * BQ : 0;
@@ -407,8 +409,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         mbar_arrive_expect_tx(k_full, 2 * L::TK);
 #pragma unroll
         for (int h = 0; h < D / 64; ++h) {
-          tma_load_3d(sb + L::OFF_KA + h * BK * 128, SETTING == 1 ? &mk1 : &mk2, k_full, h * 64, k0, bh);
-          tma_load_3d(sb + L::OFF_KB + h * BK * 128, SETTING == 1 ? &mk2 : &mk1, k_full, h * 64, k0, bh);
+          tma_load_4d(sb + L::OFF_KA + h * BK * 128, SETTING == 1 ? &mk1 : &mk2, k_full, h * 64, k0, mh, mb);
+          tma_load_4d(sb + L::OFF_KB + h * BK * 128, SETTING == 1 ? &mk2 : &mk1, k_full, h * 64, k0, mh, mb);
         }
         const CUtensorMap* mqa = SETTING == 1 ? &mq1 : &mq2;
         int issued = 0;
@@ -418,8 +420,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           mbar_arrive_expect_tx(qt_full + 8 * s, L::TQ);
 #pragma unroll
           for (int h = 0; h < D / 64; ++h)
-            tma_load_3d(sb + L::OFF_QT + s * L::TQ + h * BQ * 128, mqa, qt_full + 8 * s, h * 64, q_begin + j * BQ,
-                        bh);
+            tma_load_4d(sb + L::OFF_QT + s * L::TQ + h * BQ * 128, mqa, qt_full + 8 * s, h * 64, q_begin + j * BQ, mh, mb);
           issued = j + 1;
         }
         mbar_drain(k_full, 0, status);
@@ -438,8 +439,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           mbar_arrive_expect_tx(qo_full + 8 * s, L::TQ);
 #pragma unroll
           for (int h = 0; h < D / 64; ++h)
-            tma_load_3d(sb + L::OFF_QO + s * L::TQ + h * BQ * 128, mqb, qo_full + 8 * s, h * 64, q_begin + j * BQ,
-                        bh);
+            tma_load_4d(sb + L::OFF_QO + s * L::TQ + h * BQ * 128, mqb, qo_full + 8 * s, h * 64, q_begin + j * BQ, mh, mb);
           issued = j + 1;
         }
         for (int j = max(0, issued - SLOTS); j < issued; ++j)
@@ -601,7 +601,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       tmem_ld_wait();
       reg_fence32(g0);
       if (key < p.NK) {
-        __nv_bfloat16* dst = dk_out + ((size_t)bh * p.NK + key) * D + grp * 32;
+        __nv_bfloat16* dst = dk_out + row_offset(bh, p.H, key, p.ks_b, p.ks_h, p.ks_n) + grp * 32;
 #pragma unroll
         for (int v = 0; v < 4; ++v) {
           const uint32_t* src = &g0[v * 8];
@@ -628,8 +628,8 @@ constexpr int kOneBlockPerSmSmem = 120 * 1024;  // a block owns all 512 TMEM col
 template <int D, int SETTING>
 cudaError_t launch_dq(const Problem& p, const BwdIn& in, void* dq, int* status, cudaStream_t st) {
   CUtensorMap mx1, mx2, my1, my2;
-  if (!encode_tile_map(&mx1, in.q1, D, p.NQ, p.BH, BX) || !encode_tile_map(&mx2, in.q2, D, p.NQ, p.BH, BX) ||
-      !encode_tile_map(&my1, in.k1, D, p.NK, p.BH, BY) || !encode_tile_map(&my2, in.k2, D, p.NK, p.BH, BY))
+  if (!encode_q_map(&mx1, in.q1, p, BX) || !encode_q_map(&mx2, in.q2, p, BX) ||
+      !encode_k_map(&my1, in.k1, p, BY) || !encode_k_map(&my2, in.k2, p, BY))
     return cudaErrorInvalidValue;
   const int smem = Smem<D>::BYTES > kOneBlockPerSmSmem ? Smem<D>::BYTES : kOneBlockPerSmSmem;
   auto kern = bwd_dq_kernel<D, SETTING>;
@@ -644,8 +644,8 @@ cudaError_t launch_dq(const Problem& p, const BwdIn& in, void* dq, int* status, 
 template <int D, int SETTING>
 cudaError_t launch_dk(const Problem& p, const BwdIn& in, void* dk, int* status, cudaStream_t st) {
   CUtensorMap mk1, mk2, mq1, mq2;
-  if (!encode_tile_map(&mk1, in.k1, D, p.NK, p.BH, dkk::BK) || !encode_tile_map(&mk2, in.k2, D, p.NK, p.BH, dkk::BK) ||
-      !encode_tile_map(&mq1, in.q1, D, p.NQ, p.BH, dkk::BQ) || !encode_tile_map(&mq2, in.q2, D, p.NQ, p.BH, dkk::BQ))
+  if (!encode_k_map(&mk1, in.k1, p, dkk::BK) || !encode_k_map(&mk2, in.k2, p, dkk::BK) ||
+      !encode_q_map(&mq1, in.q1, p, dkk::BQ) || !encode_q_map(&mq2, in.q2, p, dkk::BQ))
     return cudaErrorInvalidValue;
   const int smem = dkk::Smem<D>::BYTES > kOneBlockPerSmSmem ? dkk::Smem<D>::BYTES : kOneBlockPerSmSmem;
   auto kern = bwd_dk_kernel<D, SETTING>;

@@ -140,6 +140,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_qt = (p.NQ + BM - 1) / BM;
   const int bh = blockIdx.x % p.BH;
+  const int mh = bh % p.H, mb = bh / p.H;  // head and batch coordinates of the tensor maps
   const int qt = n_qt - 1 - (int)(blockIdx.x / p.BH);  // longest causal tiles first
   const int q0 = qt * BM;
   const int q_last = min(p.NQ, q0 + BM) - 1;
@@ -183,8 +184,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_arrive_expect_tx(bar_q, 2 * L::Q_BYTES);
 #pragma unroll
       for (int h = 0; h < D / 64; ++h) {
-        tma_load_3d(sb + L::OFF_Q1 + h * BM * 128, &mq1, bar_q, h * 64, q0, bh);
-        tma_load_3d(sb + L::OFF_Q2 + h * BM * 128, &mq2, bar_q, h * 64, q0, bh);
+        tma_load_4d(sb + L::OFF_Q1 + h * BM * 128, &mq1, bar_q, h * 64, q0, mh, mb);
+        tma_load_4d(sb + L::OFF_Q2 + h * BM * 128, &mq2, bar_q, h * 64, q0, mh, mb);
       }
       int issued = 0;
       for (int j = 0; j < n_kt; ++j) {
@@ -194,8 +195,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         mbar_arrive_expect_tx(bar_full + 8 * s, L::STAGE);
 #pragma unroll
         for (int h = 0; h < D / 64; ++h) {
-          tma_load_3d(kb + h * BN * 128, &mk1, bar_full + 8 * s, h * 64, j * BN, bh);
-          tma_load_3d(kb + L::K_BYTES + h * BN * 128, &mk2, bar_full + 8 * s, h * 64, j * BN, bh);
+          tma_load_4d(kb + h * BN * 128, &mk1, bar_full + 8 * s, h * 64, j * BN, mh, mb);
+          tma_load_4d(kb + L::K_BYTES + h * BN * 128, &mk2, bar_full + 8 * s, h * 64, j * BN, mh, mb);
         }
         issued = j + 1;
       }
@@ -312,8 +313,8 @@ template <int D>
 cudaError_t launch_d(const Problem& p, const void* q1, const void* k1, const void* q2, const void* k2, float* kl,
                      float* lse1, float* lse2, int* status, cudaStream_t st) {
   CUtensorMap mq1, mk1, mq2, mk2;
-  if (!encode_tile_map(&mq1, q1, D, p.NQ, p.BH, BM) || !encode_tile_map(&mq2, q2, D, p.NQ, p.BH, BM) ||
-      !encode_tile_map(&mk1, k1, D, p.NK, p.BH, BN) || !encode_tile_map(&mk2, k2, D, p.NK, p.BH, BN))
+  if (!encode_q_map(&mq1, q1, p, BM) || !encode_q_map(&mq2, q2, p, BM) ||
+      !encode_k_map(&mk1, k1, p, BN) || !encode_k_map(&mk2, k2, p, BN))
     return cudaErrorInvalidValue;
   // A block owns all 512 TMEM columns: ask for enough shared memory that a
   // second block never shares the SM (it would only wait in tcgen05.alloc).

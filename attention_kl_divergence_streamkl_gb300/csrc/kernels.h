@@ -15,11 +15,27 @@ struct Problem {
   int off;      // NK - NQ: row i keeps key j iff j <= i + off (causal)
   float scale;  // softmax scale applied to Q K^T
   float c;      // scale * log2(e)
+  // element strides of Q1/Q2 (and dQ) and of K1/K2 (and dK) along b, h, n; d is contiguous
+  long long qs_b, qs_h, qs_n, ks_b, ks_h, ks_n;
 };
 
-// Builds a 3-D TMA map over a [BH, N, D] bf16 tensor with a {64, box_rows, 1}
-// box and the 128-byte swizzle.  Returns false if the driver rejects it.
-bool encode_tile_map(CUtensorMap* map, const void* base, int D, int N, int BH, int box_rows);
+// Element offset of row n of head (b, h) = bh in a tensor with strides (sb, sh, sn).
+__host__ __device__ inline long long row_offset(int bh, int H, long long n, long long sb, long long sh, long long sn) {
+  return (long long)(bh / H) * sb + (long long)(bh % H) * sh + n * sn;
+}
+
+// Builds a 4-D TMA map {d, n, h, b} over a bf16 [B, H, N, D] view with the given
+// element strides (d contiguous), a {64, box_rows, 1, 1} box and the 128-byte
+// swizzle.  Returns false if the driver rejects it.
+bool encode_tile_map(CUtensorMap* map, const void* base, int D, int N, int H, int B, long long sn, long long sh,
+                     long long sb, int box_rows);
+// The maps of Q1/Q2 and K1/K2 of a problem.
+inline bool encode_q_map(CUtensorMap* map, const void* base, const Problem& p, int box_rows) {
+  return encode_tile_map(map, base, p.D, p.NQ, p.H, p.B, p.qs_n, p.qs_h, p.qs_b, box_rows);
+}
+inline bool encode_k_map(CUtensorMap* map, const void* base, const Problem& p, int box_rows) {
+  return encode_tile_map(map, base, p.D, p.NK, p.H, p.B, p.ks_n, p.ks_h, p.ks_b, box_rows);
+}
 
 // ---- forward (one CTA per 128-row query tile) -------------------------------
 cudaError_t launch_fwd(const Problem& p, const void* q1, const void* k1, const void* q2, const void* k2,

@@ -113,6 +113,7 @@ __global__ void __launch_bounds__(THREADS)
   const uint32_t sb = smem_u32(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int bh = blockIdx.x;
+  const int mh = bh % p.H, mb = bh / p.H;  // head and batch coordinates of the tensor maps
   const int split = blockIdx.y, S = gridDim.y;
   const int T = (p.NK + BN - 1) / BN;
   const int t_begin = (int)(((long long)split * T) / S);
@@ -132,7 +133,7 @@ __global__ void __launch_bounds__(THREADS)
       const int r = rem / (D / 8), ch = rem % (D / 8);
       uint4 v = make_uint4(0, 0, 0, 0);
       if (r < p.NQ) {
-        const __nv_bfloat16* src = (which == 0 ? q1 : q2) + ((size_t)bh * p.NQ + r) * D + ch * 8;
+        const __nv_bfloat16* src = (which == 0 ? q1 : q2) + row_offset(bh, p.H, r, p.qs_b, p.qs_h, p.qs_n) + ch * 8;
         v = *reinterpret_cast<const uint4*>(src);
       }
       const uint32_t dst = sw128<QROWS>(sb + (which == 0 ? L::OFF_Q1 : L::OFF_Q2), r, ch);
@@ -163,8 +164,8 @@ __global__ void __launch_bounds__(THREADS)
         mbar_arrive_expect_tx(bar_full + 8 * s, L::STAGE_BYTES);
 #pragma unroll
         for (int h = 0; h < D / 64; ++h) {
-          tma_load_3d(kb + h * BN * 128, &mk1, bar_full + 8 * s, h * 64, y, bh);
-          tma_load_3d(kb + L::K_BYTES + h * BN * 128, &mk2, bar_full + 8 * s, h * 64, y, bh);
+          tma_load_4d(kb + h * BN * 128, &mk1, bar_full + 8 * s, h * 64, y, mh, mb);
+          tma_load_4d(kb + L::K_BYTES + h * BN * 128, &mk2, bar_full + 8 * s, h * 64, y, mh, mb);
         }
         issued = it + 1;
       }
@@ -326,7 +327,7 @@ template <int D>
 cudaError_t launch_d(const Problem& p, const void* q1, const void* k1, const void* q2, const void* k2, int splits,
                      float* partials, float* kl, float* lse1, float* lse2, int* status, cudaStream_t st) {
   CUtensorMap mk1, mk2;
-  if (!encode_tile_map(&mk1, k1, D, p.NK, p.BH, BN) || !encode_tile_map(&mk2, k2, D, p.NK, p.BH, BN))
+  if (!encode_k_map(&mk1, k1, p, BN) || !encode_k_map(&mk2, k2, p, BN))
     return cudaErrorInvalidValue;
   const int smem = Smem<D>::BYTES;
   cudaError_t e = cudaFuncSetAttribute(splitk_partial_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);

@@ -61,6 +61,8 @@ def parse():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--heads", type=int, default=0, help="override H (smaller cases for profiling)")
     ap.add_argument("--batch", type=int, default=0, help="override B (smaller cases for profiling)")
+    ap.add_argument("--layout", default="bhnd", choices=["bhnd", "bnhd"],
+                    help="storage of Q/K: contiguous [B,H,N,D], or [B,N,H,D] read in place through strides")
     return ap.parse_args()
 
 
@@ -276,8 +278,18 @@ def run_ours(args):
                               w.causal)
     inp = synth.make_inputs(w)
     host = [torch.from_numpy(inp[k].view(np.int16)).view(torch.bfloat16) for k in ("q1", "k1", "q2", "k2")]
+    if args.layout == "bnhd":  # same values stored [B, N, H, D], viewed as [B, H, N, D]
+        host = [t.permute(0, 2, 1, 3).contiguous().permute(0, 2, 1, 3) for t in host]
     host_g = torch.from_numpy(inp["g"])
-    q1, k1, q2, k2 = (t.to(dev) for t in host)
+
+    def like(t, pinned=False):
+        """An empty tensor with t's shape and storage order."""
+        perm = (0, 2, 1, 3) if args.layout == "bnhd" else (0, 1, 2, 3)
+        shp = tuple(t.shape[i] for i in perm)
+        e = torch.empty(shp, dtype=t.dtype, pin_memory=True) if pinned else torch.empty(shp, dtype=t.dtype, device=dev)
+        return e.permute(*perm)
+
+    q1, k1, q2, k2 = (like(t).copy_(t) for t in host)
     g = host_g.to(dev)
     scale, causal = w.softmax_scale, w.causal
     pairs = w.unmasked_pairs()
@@ -386,14 +398,14 @@ def run_ours(args):
     # ---- end to end through the public API with host buffers
     e2e = None
     if not args.no_e2e:
-        pinned = [t.pin_memory() for t in host]
+        pinned = [like(t, pinned=True).copy_(t) for t in host]
         pg = host_g.pin_memory()
         out_host = torch.empty((w.B, w.H, w.NQ), dtype=torch.float32).pin_memory()
         # Inputs stream in as in a training loop: a copy stream fills one of two device
         # input sets while the compute stream works on the other.  Every step's
         # host->device copy and its result's read-back lie inside the timed region.
         copy_stream = torch.cuda.Stream(dev)
-        bufs = [[torch.empty_like(t, device=dev) for t in pinned] for _ in range(2)]
+        bufs = [[like(t) for t in pinned] for _ in range(2)]
         gbufs = [torch.empty_like(pg, device=dev) for _ in range(2)]
         ready = [torch.cuda.Event() for _ in range(2)]
         freed = [torch.cuda.Event() for _ in range(2)]
@@ -445,7 +457,7 @@ def run_ours(args):
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": w.name, "B": w.B, "H": w.H, "N_Q": w.NQ, "N_K": w.NK, "D": w.D,
                        "causal": w.causal, "setting": args.setting if not decode else None,
-                       "bwd_path": None if decode else {1: "fused", 2: "separate"}[mode],
+                       "layout": args.layout, "bwd_path": None if decode else {1: "fused", 2: "separate"}[mode],
                        "path": ("nonsplit" if args.nonsplit else "splitk") if decode else "fwd+bwd",
                        "per_gpu_units": "the whole workload on every rank (independent heads)",
                        "l2": "inputs larger than L2, no flush between steps",

@@ -17,8 +17,9 @@
  *
  * Conventions shared by every entry point
  * ---------------------------------------
- * - Q_t are [B, H, N_Q, D] and K_t are [B, H, N_K, D], bf16, contiguous,
- *   DEVICE pointers, 16-byte aligned.  D is 64 or 128.
+ * - Q_t are [B, H, N_Q, D] and K_t are [B, H, N_K, D], bf16, DEVICE
+ *   pointers, 16-byte aligned, contiguous unless the shape's strides say
+ *   otherwise (see streamkl_shape).  D is 64 or 128.
  * - Row outputs and inputs (KL, LSE1, LSE2, g) are fp32 [B, H, N_Q], device.
  * - Gradient outputs are bf16 in the layout of the tensor they belong to.
  * - scale <= 0 selects 1/sqrt(D).  causal != 0 keeps key j for row i iff
@@ -52,17 +53,31 @@ typedef enum {
   STREAMKL_ERR_SCRATCH_LIMIT = 6 /* needs more than the fixed scratch of streamkl_fwd_splitk_noalloc */
 } streamkl_status;
 
-/* Problem shape.  scale <= 0 means 1/sqrt(D). */
+/*
+ * Problem shape.  scale <= 0 means 1/sqrt(D).
+ *
+ * q_stride_* and k_stride_* are ELEMENT strides along b, h and n of the
+ * logical [B, H, N, D] views of Q1/Q2 and of K1/K2 (D itself is contiguous).
+ * All three zero selects the contiguous [B, H, N, D] layout; otherwise each is
+ * positive and a multiple of 8 (16 bytes), n's stride is at least D, and both
+ * tensors of a pair (Q1 and Q2, K1 and K2) share the strides.  A [B, N, H, D]
+ * tensor, as many attention implementations store it, is passed without a
+ * copy as strides (N*H*D, D, H*D).  Gradient outputs (dQ, dK) are written
+ * with the strides of the input they belong to; row-shaped tensors (KL, LSE,
+ * g) stay contiguous [B, H, N_Q].
+ */
 typedef struct {
   int B, H, NQ, NK, D;
   float scale;
   int causal;
+  long long q_stride_b, q_stride_h, q_stride_n;
+  long long k_stride_b, k_stride_h, k_stride_n;
 } streamkl_shape;
 
 /* Backward path selection (the adaptive rule of section 手法 2 "kernel fusion"). */
 typedef enum {
   STREAMKL_BWD_AUTO = 0,     /* fused when the live rows of the fp32 dK buffer fit in L2, else separate */
-  STREAMKL_BWD_FUSED = 1,    /* one pass over each QK tile pair, dQ by atomics into fp32 */
+  STREAMKL_BWD_FUSED = 1,    /* one pass over each QK tile pair, dQ on chip, dK by atomics into fp32 */
   STREAMKL_BWD_SEPARATE = 2, /* a Q-stationary dQ kernel and a K-stationary dK kernel */
   STREAMKL_BWD_DQ_ONLY = 3,  /* separate path, dQ kernel only (dK pointer may be NULL) */
   STREAMKL_BWD_DK_ONLY = 4   /* separate path, dK kernel only (dQ pointer may be NULL) */

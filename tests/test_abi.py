@@ -171,3 +171,46 @@ def test_bwd_select_rule(lib):
     assert K.bwd_select(64, 32, 256, 4096, 128, 77 * 4096 * 512 - 1, sms) == K.BWD_SEPARATE
     assert K.bwd_select(0, 1, 8, 8, 64, l2, sms) == 0  # invalid shape
     assert K.bwd_select(1, 1, 8, 8, 64, l2, 0) == 0  # no SM count
+
+
+@pytest.mark.parametrize("qs,ks,code", [
+    ((0, 0, 0), (0, 0, 0), K.OK),                                   # contiguous
+    ((64 * 4 * 128, 128, 4 * 128), (4096 * 4 * 128, 128, 4 * 128), K.OK),  # [B, N, H, D] views
+    ((0, 0, 0), (3 * 4096 * 4 * 128, 128, 3 * 4 * 128), K.OK),      # K sliced from a packed [B, N, 3, H, D]
+    ((64 * 4 * 128, 128, 64), (0, 0, 0), K.ERR_INVALID),            # rows shorter than D
+    ((64 * 4 * 128, 128, 4 * 128 + 4), (0, 0, 0), K.ERR_INVALID),   # not a multiple of 8 elements
+    ((0, 0, 0), (-128, 128, 512), K.ERR_INVALID),                   # negative
+    ((0, 0, 128), (0, 0, 0), K.ERR_INVALID),                        # partly zero
+    ((1 << 38, 128, 512), (0, 0, 0), K.ERR_INVALID),                # beyond the tensor map's stride range
+])
+def test_stride_validation(lib, qs, ks, code):
+    s = K.make_shape(2, 4, 64, 4096, 128, q_strides=qs, k_strides=ks)
+    n = ctypes.c_size_t()
+    assert lib.streamkl_bwd_workspace(s, K.BWD_SEPARATE, ctypes.byref(n)) == code
+    if code != K.OK:  # the compute entry points refuse the same shapes before any launch
+        assert call_fwd(lib, s) == code
+
+
+def test_binding_reads_views_in_place():
+    torch = pytest.importorskip("torch")
+    np = pytest.importorskip("numpy")
+    B_, N, H, D = 2, 48, 4, 64
+    bnhd = torch.zeros(B_, N, H, D, dtype=torch.bfloat16)
+    assert K._bhn_strides(bnhd.permute(0, 2, 1, 3)) == (N * H * D, D, H * D)
+    qkv = torch.zeros(B_, N, 3, H, D, dtype=torch.bfloat16)
+    assert K._bhn_strides(qkv[:, :, 1].permute(0, 2, 1, 3)) == (N * 3 * H * D, D, 3 * H * D)
+    c = torch.zeros(B_, H, N, D, dtype=torch.bfloat16)
+    assert K._bhn_strides(c) == (H * N * D, N * D, D)
+    assert K._bhn_strides(c[:1, :1]) == (8, 8, D)  # extent-1 strides replaced by valid ones
+    assert K._bhn_strides(c.transpose(2, 3)) is None  # D not contiguous
+    buf = torch.zeros(B_ * H * N * D + 8, dtype=torch.bfloat16)
+    assert K._bhn_strides(buf[4:4 + B_ * H * N * D].view(B_, H, N, D)) is None  # start not 16-byte aligned
+    assert K._bhn_strides(c[:, :1].expand(B_, H, N, D)) is None  # zero stride
+    assert K._bhn_strides(torch.as_strided(c, (B_, H, N, D), (H * N * D, N * D, 8, 1))) is None  # overlapping rows
+    empty = torch.from_numpy(np.zeros((1, 2, 0, 64), np.int16)).view(torch.bfloat16)  # numpy gives zero strides
+    assert K._bhn_strides(empty) == (2 * 64, 64, 64)
+    # a mismatched pair is made contiguous together
+    a, b, st = K._pair(bnhd.permute(0, 2, 1, 3), c)
+    assert a.is_contiguous() and b.is_contiguous() and st == (H * N * D, N * D, D)
+    g = K._grad_like(qkv[:, :, 0].permute(0, 2, 1, 3), (N * 3 * H * D, D, 3 * H * D), N)
+    assert g.stride() == (N * 3 * H * D, D, 3 * H * D, 1)
