@@ -201,8 +201,10 @@ __global__ void __launch_bounds__(THREADS, 1)
       __syncwarp();
     } else if (warp == MMA_WARP) {
       // ------------------------------------------------------------------ MMA issuer
-      // Per key tile j: S_a(j), S_b(j) (once the dS warps hold S_a(j)), then dQ and
-      // dKp of tile j - 1, whose dS is ready by the time S_b(j) is done.
+      // Per key tile j: S_a(j); dQ of tile j - 1 (its dS is done before the dS warps
+      // read S_a(j), so it fills the tensor pipe while they do); S_b(j) once they
+      // hold S_a(j); then dKp of tile j - 1.  S_a(j + 1) then queues behind one
+      // gradient group, not two, and K_opt(j - 1) is released before S_b(j).
       if (lane == 0) {
         constexpr uint32_t id_s = idesc_bf16(BQ, BK, false, false);
         constexpr uint32_t id_dq = idesc_bf16(BQ, D, false, true);
@@ -213,8 +215,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         const uint64_t dsm = sdesc_sw128(sb + L::OFF_DS, BQ * 128, 1024);  // dS as B of dKp (MN-major over keys)
         bool ok = mbar_wait(q_full, 0, status, abort_flag);
         for (int j = 0; ok && j <= n_kt; ++j) {
+          const int s = j % SLOTS;
           if (j < n_kt) {
-            const int s = j % SLOTS;
             if (!mbar_wait(kt_full + 8 * s, (j / SLOTS) & 1, status, abort_flag)) break;
             if (j >= 1 && !mbar_wait(sb_free, (j - 1) & 1, status, abort_flag)) break;
             tc_fence_after();
@@ -226,6 +228,20 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             mma_commit(sa_full);
             mma_commit(kt_empty + 8 * s);  // the other K tile is read only by S_a
+          }
+          if (j >= 1) {
+            const int jj = j - 1, sp = jj % SLOTS;
+            if (!mbar_wait(ds_full, jj & 1, status, abort_flag)) break;
+            tc_fence_after();
+            // dQ += dS K_opt: A = dS[query][key] K-major (key k-steps), B = K_opt read MN-major
+            const uint64_t kod = sdesc_sw128(sb + L::OFF_KO + sp * L::TK, BK * 128, 1024);
+#pragma unroll
+            for (int ks = 0; ks < BK / 16; ++ks)
+              mma_ss(tmem + kColDQ, sdesc_add(dsk, (ks >> 2) * (BQ * 128) + (ks & 3) * 32), sdesc_add(kod, ks * 2048),
+                     id_dq, jj > 0 || ks > 0);
+            mma_commit(ko_empty + 8 * sp);  // K_opt(jj) was read by S_b(jj) and this dQ
+          }
+          if (j < n_kt) {
             if (!mbar_wait(sa_free, j & 1, status, abort_flag)) break;
             if (!mbar_wait(ko_full + 8 * s, (j / SLOTS) & 1, status, abort_flag)) break;
             tc_fence_after();
@@ -238,22 +254,14 @@ __global__ void __launch_bounds__(THREADS, 1)
             mma_commit(sb_full);
           }
           if (j >= 1) {
-            const int jj = j - 1, s = jj % SLOTS, b = jj & 1;
-            if (!mbar_wait(ds_full, jj & 1, status, abort_flag)) break;
+            const int jj = j - 1, b = jj & 1;
             // dKp^T buffer b was drained (tile jj - 2) by the dK warps
             if (jj >= 2 && !mbar_wait(dk_free + 8 * b, ((jj >> 1) - 1) & 1, status, abort_flag)) break;
             tc_fence_after();
-            // dQ += dS K_opt: A = dS[query][key] K-major (key k-steps), B = K_opt read MN-major
-            const uint64_t kod = sdesc_sw128(sb + L::OFF_KO + s * L::TK, BK * 128, 1024);
-#pragma unroll
-            for (int ks = 0; ks < BK / 16; ++ks)
-              mma_ss(tmem + kColDQ, sdesc_add(dsk, (ks >> 2) * (BQ * 128) + (ks & 3) * 32), sdesc_add(kod, ks * 2048),
-                     id_dq, jj > 0 || ks > 0);
             // dKp^T = Q_opt^T dS: A = Q_opt (queries x d) read MN-major, B = dS (queries x keys) MN-major
 #pragma unroll
             for (int ks = 0; ks < BQ / 16; ++ks)
               mma_ss(tmem + kColDK + 128 * b, sdesc_add(qod, ks * 2048), sdesc_add(dsm, ks * 2048), id_dk, ks > 0);
-            mma_commit(ko_empty + 8 * s);
             mma_commit(ds_free);
             mma_commit(dk_full + 8 * b);
           }
