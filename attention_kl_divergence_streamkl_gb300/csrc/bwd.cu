@@ -334,6 +334,16 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (lane == 0) mbar_arrive(sa_free);
       const int kg = j * BK + grp * 32;
       const bool masked = (kg + 31 >= p.NK) || (row >= p.NQ) || (p.causal && kg + 31 > row + p.off);
+      const uint32_t vis = masked ? visible_keys<16>(row, kg, p.NQ, p.NK, p.off, p.causal) |
+                                        (visible_keys<16>(row, kg + 16, p.NQ, p.NK, p.off, p.causal) << 16)
+                                  : ~0u;
+      if (SETTING == 1) {
+        // P1 needs S_a (= S1) alone: computed in place while S_b is computed
+        if (masked)
+          p1_row<true, 32>(held, c, nAr, vis);
+        else
+          p1_row<false, 32>(held, c, nAr, 0u);
+      }
       uint32_t pk[16];
       ok = mbar_wait(sb_full, j & 1, status, abort_flag);
       __syncwarp();
@@ -352,17 +362,17 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (lane == 0) mbar_arrive(sb_free);
         }
         const uint32_t(&ha)[16] = *reinterpret_cast<const uint32_t(*)[16]>(&held[16 * h]);
-        auto run = [&](const uint32_t(&s1)[16], const uint32_t(&s2)[16]) {
+        if (SETTING == 1) {  // S_b = S2; held = P1
           if (masked)
-            make_ds_row<SETTING, true, 16>(s1, s2, pk + 8 * h, c, p.scale, nAr, nBr, Gr,
-                                           visible_keys<16>(row, kg + 16 * h, p.NQ, p.NK, p.off, p.causal));
+            ds1_from_p1<true, 16>(half, ha, pk + 8 * h, c, nBr, Gr, vis >> (16 * h));
           else
-            make_ds_row<SETTING, false, 16>(s1, s2, pk + 8 * h, c, p.scale, nAr, nBr, Gr, 0u);
-        };
-        if (SETTING == 1)
-          run(ha, half);  // S_a = S1, S_b = S2
-        else
-          run(half, ha);  // S_a = S2, S_b = S1
+            ds1_from_p1<false, 16>(half, ha, pk + 8 * h, c, nBr, Gr, 0u);
+        } else {  // S_a = S2, S_b = S1
+          if (masked)
+            make_ds_row<SETTING, true, 16>(half, ha, pk + 8 * h, c, p.scale, nAr, nBr, Gr, vis >> (16 * h));
+          else
+            make_ds_row<SETTING, false, 16>(half, ha, pk + 8 * h, c, p.scale, nAr, nBr, Gr, 0u);
+        }
         if (h == 0)  // first half final before the second half is read
           asm volatile("" : "+r"(pk[0]), "+r"(pk[1]), "+r"(pk[2]), "+r"(pk[3]), "+r"(pk[4]), "+r"(pk[5]),
                        "+r"(pk[6]), "+r"(pk[7])::"memory");
@@ -435,7 +445,6 @@ cudaError_t launch_fused(const Problem& p, const BwdIn& in, void* dq, float* dk_
   return cudaGetLastError();
 }
 
-// dK (bf16) = scale * dK accumulator (fp32); 8 elements per thread.
 // dK = scale * acc, rounded to bf16 and written with dK's own strides; acc is
 // the contiguous fp32 [B*H, N_K, D] accumulator.  One thread converts 8 values.
 template <int D>

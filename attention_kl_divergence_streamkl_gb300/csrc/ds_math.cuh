@@ -72,4 +72,41 @@ __device__ __forceinline__ void make_ds_row(const uint32_t (&a)[N], const uint32
   }
 }
 
+// Setting 1 in two steps, for kernels that receive S1 before S2.  First, in
+// place: P1 for N columns of S1 (0 where the key is not visible).
+template <bool MASKED, int N>
+__device__ __forceinline__ void p1_row(uint32_t (&s)[N], float c, float nAr, uint32_t visible) {
+  const float2 cc = make_float2(c, c), nA = make_float2(nAr, nAr);
+#pragma unroll
+  for (int k = 0; k < N; k += 2) {
+    const float2 x1 = ffma2(make_float2(__uint_as_float(s[k]), __uint_as_float(s[k + 1])), cc, nA);
+    float2 p1 = make_float2(ex2(x1.x), ex2(x1.y));
+    if (MASKED) {
+      p1.x = (visible >> k) & 1u ? p1.x : 0.f;
+      p1.y = (visible >> (k + 1)) & 1u ? p1.y : 0.f;
+    }
+    s[k] = __float_as_uint(p1.x);
+    s[k + 1] = __float_as_uint(p1.y);
+  }
+}
+
+// Then dS2 = g (P2 - P1) for N columns, from S2 and the first step's P1 (the
+// same operations as ds_pair, so identical distributions give exact zeros).
+template <bool MASKED, int N>
+__device__ __forceinline__ void ds1_from_p1(const uint32_t (&s2)[N], const uint32_t* p1v, uint32_t* pk, float c,
+                                            float nBr, float Gr, uint32_t visible) {
+  const float2 cc = make_float2(c, c), nB = make_float2(nBr, nBr), G = make_float2(Gr, Gr);
+#pragma unroll
+  for (int k = 0; k < N; k += 2) {
+    const float2 x2 = ffma2(make_float2(__uint_as_float(s2[k]), __uint_as_float(s2[k + 1])), cc, nB);
+    float2 p2 = make_float2(ex2(x2.x), ex2(x2.y));
+    if (MASKED) {
+      p2.x = (visible >> k) & 1u ? p2.x : 0.f;
+      p2.y = (visible >> (k + 1)) & 1u ? p2.y : 0.f;
+    }
+    const float2 ds = fmul2(G, fsub2(p2, make_float2(__uint_as_float(p1v[k]), __uint_as_float(p1v[k + 1]))));
+    pk[k / 2] = pack_bf16(ds.x, ds.y);
+  }
+}
+
 }  // namespace skl
