@@ -16,8 +16,10 @@
 //   dQ   += dS K_opt                    SS: A = dS (K-major over keys), B = K_opt MN-major  -> [128, 128 + D)
 //   dKp^T = Q_opt^T dS                  SS: A = Q_opt read MN-major (M = d), B = dS MN-major -> [256 + 128 b, ...)
 //   dk_acc[key, d] += dKp^T[d, key]     one warp adds 32 consecutive d of one key row (128 B) per red
-// The dS warps copy S_a into registers, S_b is written over it and read in two
-// halves.  A thread owns a query row, so its per-query values sit in registers
+// The MMAs of key tile j are issued as S_a(j), dQ(j - 1), S_b(j), dKp(j - 1).
+// The dS warps copy S_a into registers (in setting 1 they turn it into P1 while
+// S_b is in flight), S_b is written over it and read in two halves.  A thread
+// owns a query row, so its per-query values sit in registers
 // and the dS loop issues no shared-memory loads; the dK warps' reductions,
 // bounded by L2 reduction throughput, overlap it instead of competing for the
 // LSU.  dKp^T is double-buffered so they have two tile periods per tile.
