@@ -63,8 +63,9 @@ typedef enum {
  * tensors of a pair (Q1 and Q2, K1 and K2) share the strides.  A [B, N, H, D]
  * tensor, as many attention implementations store it, is passed without a
  * copy as strides (N*H*D, D, H*D).  Gradient outputs (dQ, dK) are written
- * with the strides of the input they belong to; row-shaped tensors (KL, LSE,
- * g) stay contiguous [B, H, N_Q].
+ * with the strides of the input they belong to, so those strides must not
+ * make two rows overlap (inputs are only read and may overlap); row-shaped
+ * tensors (KL, LSE, g) stay contiguous [B, H, N_Q].
  */
 typedef struct {
   int B, H, NQ, NK, D;
