@@ -56,6 +56,7 @@ SIGNATURES = {
     "streamkl_fwd_splitk_noalloc": (_I, [_P, _P, _P, _P, Shape, _I, _F, _F, _F, _S]),
     "streamkl_bwd_workspace": (_I, [Shape, _I, ctypes.POINTER(_SZ)]),
     "streamkl_bwd_select": (_I, [Shape, _SZ, _I]),
+    "streamkl_bwd_fused_plan": (_I, [Shape, _SZ, _I, ctypes.POINTER(_I), ctypes.POINTER(_SZ)]),
     "streamkl_bwd_s1": (_I, [_P, _P, _P, _P, Shape, _F, _F, _F, _P, _P, _I, _P, _SZ, _S]),
     "streamkl_bwd_s2": (_I, [_P, _P, _P, _P, Shape, _F, _F, _F, _F, _P, _P, _I, _P, _SZ, _S]),
     "streamkl_status_string": (ctypes.c_char_p, [_I]),
@@ -227,6 +228,14 @@ def fwd_splitk(q1, k1, q2, k2, scale=None, causal=False, num_splits=0):
 
 def bwd_select(B, H, NQ, NK, D, l2_bytes, num_sms, causal=False) -> int:
     return lib().streamkl_bwd_select(make_shape(B, H, NQ, NK, D, None, causal), int(l2_bytes), int(num_sms))
+
+
+def bwd_fused_plan(B, H, NQ, NK, D, l2_bytes, num_sms, causal=False):
+    """(key ranges, workspace bytes) of the fused backward on a device with this L2 and SM count."""
+    n, ws = ctypes.c_int(0), ctypes.c_size_t(0)
+    _check(lib().streamkl_bwd_fused_plan(make_shape(B, H, NQ, NK, D, None, causal), int(l2_bytes), int(num_sms),
+                                         ctypes.byref(n), ctypes.byref(ws)), "streamkl_bwd_fused_plan")
+    return n.value, ws.value
 
 
 def bwd_workspace_bytes(B, H, NQ, NK, D, bwd_mode=BWD_AUTO, causal=False) -> int:

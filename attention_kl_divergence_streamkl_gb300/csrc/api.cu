@@ -1,5 +1,7 @@
 // C-ABI of libstreamkl: argument validation, path selection and launches.
 // The operations are declared and documented in include/streamkl.h.
+#include <cstdlib>
+#include <algorithm>
 #include <math.h>
 #include <stdint.h>
 
@@ -95,8 +97,6 @@ streamkl_status status_ptr(int** out) {
 
 streamkl_status from_cuda(cudaError_t e) { return e == cudaSuccess ? STREAMKL_OK : STREAMKL_ERR_CUDA; }
 
-size_t fused_acc_bytes(const Problem& p) { return (size_t)p.BH * p.NK * p.D * sizeof(float); }
-
 // The fused path adds dK partials into the fp32 buffer with atomics; they stay
 // cheap while the rows being accumulated stay in L2.  Its blocks run head by
 // head (all query tiles of one (b, h) before the next), so the live part of the
@@ -109,9 +109,50 @@ size_t live_acc_bytes(const Problem& p, int num_sms) {
   return (size_t)p.NK * p.D * sizeof(float) * (size_t)heads;
 }
 
-int resolve_bwd_mode(const Problem& p, int mode, size_t l2_bytes, int num_sms) {
-  if (mode == STREAMKL_BWD_FUSED || mode == STREAMKL_BWD_SEPARATE) return mode;
-  return live_acc_bytes(p, num_sms) <= l2_bytes ? STREAMKL_BWD_FUSED : STREAMKL_BWD_SEPARATE;
+// The same for one key range of `tiles` 128-key tiles: its dK rows times the
+// heads in flight, counted with the fewest query tiles any range has (the last
+// range's, under a causal mask).
+size_t live_range_bytes(const Problem& p, int tiles, int num_sms) {
+  const long long n_kt = (p.NK + 127) / 128, n_qt = (p.NQ + 127) / 128;
+  const long long ranges = (n_kt + tiles - 1) / tiles;
+  const long long keys = std::min<long long>((long long)tiles * 128, p.NK);
+  const long long query_tiles = std::max<long long>(1, n_qt - fused_first_qtile(p, (ranges - 1) * tiles * 128));
+  const long long heads_in_flight = (num_sms + query_tiles - 1) / query_tiles + 1;
+  const long long heads = heads_in_flight < p.BH ? heads_in_flight : p.BH;
+  return (size_t)keys * p.D * sizeof(float) * (size_t)heads;
+}
+
+// Key tiles per launch of the fused backward.  Its dK partials go into an fp32
+// buffer through atomics, which stay cheap while the rows being accumulated
+// stay in L2: all keys in one launch when their live rows fit, else the longest
+// key range whose live rows fit in half the L2 (the K tiles streamed for those
+// heads share it), with dQ summed over the ranges in fp32.  A positive integer
+// in the environment variable STREAMKL_FUSED_KEY_TILES overrides the choice.
+int fused_range_tiles(const Problem& p, size_t l2_bytes, int num_sms) {
+  const int n_kt = (p.NK + 127) / 128;
+  if (const char* e = std::getenv("STREAMKL_FUSED_KEY_TILES")) {
+    const long v = std::strtol(e, nullptr, 10);
+    if (v > 0) return (int)std::min<long>(v, n_kt);
+  }
+  if (live_acc_bytes(p, num_sms) <= l2_bytes) return n_kt;
+  for (int n = 2;; ++n) {
+    const int tiles = (n_kt + n - 1) / n;
+    if (tiles <= 1 || live_range_bytes(p, tiles, num_sms) <= l2_bytes / 2) return std::max(tiles, 1);
+  }
+}
+
+size_t fused_workspace_bytes(const Problem& p, int range_tiles) {
+  const long long n_kt = (p.NK + 127) / 128;
+  const size_t dk_rows = (size_t)std::min<long long>((long long)range_tiles * 128, p.NK);
+  size_t bytes = (size_t)p.BH * dk_rows * p.D * sizeof(float);
+  if (range_tiles < n_kt) bytes += (size_t)p.BH * p.NQ * p.D * sizeof(float);
+  return bytes;
+}
+
+// AUTO takes the fused path: over key ranges it keeps its atomics in L2 for any
+// N_K.  Every other mode stands as given.
+int resolve_bwd_mode(const Problem&, int mode, size_t, int) {
+  return mode == STREAMKL_BWD_AUTO ? STREAMKL_BWD_FUSED : mode;
 }
 
 streamkl_status device_l2_bytes(size_t* out) {
@@ -263,18 +304,32 @@ int streamkl_bwd_select(streamkl_shape s, size_t l2_bytes, int num_sms) {
   return resolve_bwd_mode(p, STREAMKL_BWD_AUTO, l2_bytes, num_sms);
 }
 
+streamkl_status streamkl_bwd_fused_plan(streamkl_shape s, size_t l2_bytes, int num_sms, int* key_ranges,
+                                        size_t* workspace_bytes) {
+  Problem p;
+  streamkl_status v = validate(s, &p);
+  if (v != STREAMKL_OK) return v;
+  if (num_sms <= 0 || !key_ranges || !workspace_bytes) return STREAMKL_ERR_INVALID;
+  const int tiles = fused_range_tiles(p, l2_bytes, num_sms);
+  const int n_kt = (p.NK + 127) / 128;
+  *key_ranges = (n_kt + tiles - 1) / tiles;
+  *workspace_bytes = fused_workspace_bytes(p, tiles);
+  return STREAMKL_OK;
+}
+
 streamkl_status streamkl_bwd_workspace(streamkl_shape s, int bwd_mode, size_t* bytes) {
   Problem p;
   streamkl_status v = validate(s, &p);
   if (v != STREAMKL_OK) return v;
   if (!bytes || bwd_mode < 0 || bwd_mode > STREAMKL_BWD_DK_ONLY) return STREAMKL_ERR_INVALID;
-  if (bwd_mode == STREAMKL_BWD_AUTO) {
+  bwd_mode = resolve_bwd_mode(p, bwd_mode, 0, 0);
+  *bytes = 0;
+  if (bwd_mode == STREAMKL_BWD_FUSED) {
     size_t l2 = 0;
     int sms = 0;
     if ((v = device_l2_bytes(&l2)) != STREAMKL_OK || (v = device_sms(&sms)) != STREAMKL_OK) return v;
-    bwd_mode = resolve_bwd_mode(p, bwd_mode, l2, sms);
+    *bytes = fused_workspace_bytes(p, fused_range_tiles(p, l2, sms));
   }
-  *bytes = bwd_mode == STREAMKL_BWD_FUSED ? fused_acc_bytes(p) : 0;
   return STREAMKL_OK;
 }
 
@@ -298,20 +353,22 @@ static streamkl_status bwd_common(int setting, const void* q1, const void* k1, c
     return STREAMKL_ERR_INVALID;
   if (want_dq && (!dq || !aligned16(dq))) return STREAMKL_ERR_INVALID;
   if (setting == 2 && !rows_ok(kl)) return STREAMKL_ERR_INVALID;
-  if (bwd_mode == STREAMKL_BWD_AUTO) {
+  bwd_mode = resolve_bwd_mode(p, bwd_mode, 0, 0);
+  int range_tiles = 0;
+  if (bwd_mode == STREAMKL_BWD_FUSED) {
+    if (!workspace || !aligned16(workspace)) return STREAMKL_ERR_WORKSPACE;
     size_t l2 = 0;
     int sms = 0;
     if ((v = device_l2_bytes(&l2)) != STREAMKL_OK || (v = device_sms(&sms)) != STREAMKL_OK) return v;
-    bwd_mode = resolve_bwd_mode(p, bwd_mode, l2, sms);
+    range_tiles = fused_range_tiles(p, l2, sms);
+    if (workspace_bytes < fused_workspace_bytes(p, range_tiles)) return STREAMKL_ERR_WORKSPACE;
   }
-  if (bwd_mode == STREAMKL_BWD_FUSED &&
-      (!workspace || !aligned16(workspace) || workspace_bytes < fused_acc_bytes(p)))
-    return STREAMKL_ERR_WORKSPACE;
   int* status = nullptr;
   if ((v = status_ptr(&status)) != STREAMKL_OK) return v;
   BwdIn in{q1, k1, q2, k2, lse1, lse2, kl, g};
   if (bwd_mode == STREAMKL_BWD_FUSED)
-    return from_cuda(launch_bwd_fused(p, setting, in, dq, dk, static_cast<float*>(workspace), status, st));
+    return from_cuda(
+        launch_bwd_fused(p, setting, in, dq, dk, static_cast<float*>(workspace), range_tiles, status, st));
   return from_cuda(launch_bwd_separate(p, setting, in, want_dq ? dq : nullptr, want_dk ? dk : nullptr, status, st));
 }
 

@@ -30,6 +30,7 @@
 //   warp 18     TMA producer of K_opt (two slots, each held until the gradient MMAs)
 //   warps 20-23 dK warps: thread = column d of dKp^T, reduce-add into dk_acc
 // Warpgroups 4-5 give registers to the dS warpgroups (setmaxnreg).
+#include <algorithm>
 #include <utility>
 
 #include "common.cuh"
@@ -92,11 +93,23 @@ __device__ __forceinline__ void red_rows(float* base, const uint32_t (&v)[32], i
   ((I < nrow ? red_add_at<I * D * 4>(base, __uint_as_float(v[I])) : void()), ...);
 }
 
+// One launch covers the key tiles [jt0, jt1) and the query tiles from qt_min on
+// (those that see a key of the range).  dK partials go to the range's rows of
+// dk_acc ([B*H][dk_rows][D] fp32, row = key - 128 jt0).  dQ: DQ_BF16 writes the
+// finished bf16 gradient (the range is every key), DQ_STORE / DQ_ADD store or
+// add the unscaled fp32 sum over the range into dq_acc ([B*H][N_Q][D]).
+enum { DQ_BF16 = 0, DQ_STORE = 1, DQ_ADD = 2 };
+struct KeyRange {
+  int jt0, jt1, qt_min, dq_mode, dk_rows;
+  float* dq_acc;
+};
+
 template <int D, int SETTING>
 __global__ void __launch_bounds__(THREADS, 1)
-    bwd_fused_tc_kernel(const Problem p, const float* __restrict__ lse1, const float* __restrict__ lse2,
-                        const float* __restrict__ klv, const float* __restrict__ gv,
-                        __nv_bfloat16* __restrict__ dq_out, float* __restrict__ dk_acc, int* status,
+    bwd_fused_tc_kernel(const Problem p, const KeyRange kr, const float* __restrict__ lse1,
+                        const float* __restrict__ lse2, const float* __restrict__ klv,
+                        const float* __restrict__ gv, __nv_bfloat16* __restrict__ dq_out,
+                        float* __restrict__ dk_acc, int* status,
                         const __grid_constant__ CUtensorMap mq1, const __grid_constant__ CUtensorMap mq2,
                         const __grid_constant__ CUtensorMap mk1, const __grid_constant__ CUtensorMap mk2) {
   using L = Smem<D>;
@@ -105,13 +118,15 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t sb = smem_u32(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_qt = (p.NQ + BQ - 1) / BQ;
-  const int bh = (int)(blockIdx.x / n_qt);               // heads in order (their dk_acc rows stay in L2), ...
-  const int qt = n_qt - 1 - (int)(blockIdx.x % n_qt);    // ... and within a head the longest (last) query tiles first
+  const int n_qt_r = n_qt - kr.qt_min;                   // query tiles that see this key range
+  const int bh = (int)(blockIdx.x / n_qt_r);             // heads in order (their dk_acc rows stay in L2), ...
+  const int qt = n_qt - 1 - (int)(blockIdx.x % n_qt_r);  // ... and within a head the longest (last) query tiles first
   const int mh = bh % p.H, mb = bh / p.H;  // head and batch coordinates of the tensor maps
   const int q0 = qt * BQ;
   const int q_last = min(p.NQ, q0 + BQ) - 1;
-  const int kend = p.causal ? min(p.NK, q_last + p.off + 1) : p.NK;
-  const int n_kt = (kend + BK - 1) / BK;
+  const int kend = min(p.causal ? min(p.NK, q_last + p.off + 1) : p.NK, kr.jt1 * BK);
+  const int n_kt = (kend + BK - 1) / BK - kr.jt0;  // >= 1: qt >= qt_min sees key 128 jt0
+  const int kbase = kr.jt0 * BK;                   // first key of the range; local tile j = keys kbase + 128 j
 
   const uint32_t bar = sb + L::OFF_BAR;
   const uint32_t q_full = bar, ko_full = bar + 8, ko_empty = bar + 24, kt_full = bar + 40, kt_empty = bar + 56,
@@ -173,7 +188,8 @@ __global__ void __launch_bounds__(THREADS, 1)
           mbar_arrive_expect_tx(kt_full + 8 * s, L::TK);
 #pragma unroll
           for (int h = 0; h < D / 64; ++h)
-            tma_load_4d(sb + L::OFF_KT + s * L::TK + h * BK * 128, mka, kt_full + 8 * s, h * 64, j * BK, mh, mb);
+            tma_load_4d(sb + L::OFF_KT + s * L::TK + h * BK * 128, mka, kt_full + 8 * s, h * 64, kbase + j * BK, mh,
+                        mb);
           issued = j + 1;
         }
         mbar_drain(q_full, 0, status);
@@ -194,7 +210,8 @@ __global__ void __launch_bounds__(THREADS, 1)
           mbar_arrive_expect_tx(ko_full + 8 * s, L::TK);
 #pragma unroll
           for (int h = 0; h < D / 64; ++h)
-            tma_load_4d(sb + L::OFF_KO + s * L::TK + h * BK * 128, mkb, ko_full + 8 * s, h * 64, j * BK, mh, mb);
+            tma_load_4d(sb + L::OFF_KO + s * L::TK + h * BK * 128, mkb, ko_full + 8 * s, h * 64, kbase + j * BK, mh,
+                        mb);
           issued = j + 1;
         }
         for (int j = max(0, issued - SLOTS); j < issued; ++j)
@@ -284,8 +301,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         __syncwarp();
         if (!got) break;
         tc_fence_after();
-        const int k0 = j * BK;
-        float* base = dk_acc + ((size_t)bh * p.NK + k0) * D + d;
+        const int k0 = kbase + j * BK;
+        float* base = dk_acc + ((size_t)bh * kr.dk_rows + j * BK) * D + d;
 #pragma unroll 1
         for (int cb = 0; cb < BK / 32; ++cb) {
           uint32_t v[32];
@@ -334,7 +351,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(sa_free);
-      const int kg = j * BK + grp * 32;
+      const int kg = kbase + j * BK + grp * 32;
       const bool masked = (kg + 31 >= p.NK) || (row >= p.NQ) || (p.causal && kg + 31 > row + p.off);
       const uint32_t vis = masked ? visible_keys<16>(row, kg, p.NQ, p.NK, p.off, p.causal) |
                                         (visible_keys<16>(row, kg + 16, p.NQ, p.NK, p.off, p.causal) << 16)
@@ -406,7 +423,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       tmem_ld32(tmem + lane_base + kColDQ + grp * 32, g0);
       tmem_ld_wait();
       reg_fence32(g0);
-      if (row < p.NQ) {
+      if (row < p.NQ && kr.dq_mode == DQ_BF16) {
         __nv_bfloat16* dst = dq_out + row_offset(bh, p.H, row, p.qs_b, p.qs_h, p.qs_n) + grp * 32;
 #pragma unroll
         for (int v = 0; v < 4; ++v) {
@@ -417,6 +434,21 @@ __global__ void __launch_bounds__(THREADS, 1)
           o.z = pack_bf16(__uint_as_float(src[4]) * p.scale, __uint_as_float(src[5]) * p.scale);
           o.w = pack_bf16(__uint_as_float(src[6]) * p.scale, __uint_as_float(src[7]) * p.scale);
           reinterpret_cast<uint4*>(dst)[v] = o;
+        }
+      } else if (row < p.NQ) {
+        float4* dst = reinterpret_cast<float4*>(kr.dq_acc + ((size_t)bh * p.NQ + row) * D + grp * 32);
+#pragma unroll
+        for (int v = 0; v < 8; ++v) {
+          float4 o = make_float4(__uint_as_float(g0[4 * v]), __uint_as_float(g0[4 * v + 1]),
+                                 __uint_as_float(g0[4 * v + 2]), __uint_as_float(g0[4 * v + 3]));
+          if (kr.dq_mode == DQ_ADD) {
+            const float4 a = dst[v];
+            o.x += a.x;
+            o.y += a.y;
+            o.z += a.z;
+            o.w += a.w;
+          }
+          dst[v] = o;
         }
       }
     }
@@ -432,7 +464,8 @@ __global__ void __launch_bounds__(THREADS, 1)
 constexpr int kOneBlockPerSmSmem = 120 * 1024;  // a block owns all 512 TMEM columns
 
 template <int D, int SETTING>
-cudaError_t launch_fused(const Problem& p, const BwdIn& in, void* dq, float* dk_acc, int* status, cudaStream_t st) {
+cudaError_t launch_fused(const Problem& p, const KeyRange& kr, const BwdIn& in, void* dq, float* dk_acc, int* status,
+                         cudaStream_t st) {
   CUtensorMap mq1, mq2, mk1, mk2;
   if (!encode_q_map(&mq1, in.q1, p, BQ) || !encode_q_map(&mq2, in.q2, p, BQ) ||
       !encode_k_map(&mk1, in.k1, p, BK) || !encode_k_map(&mk2, in.k2, p, BK))
@@ -441,53 +474,88 @@ cudaError_t launch_fused(const Problem& p, const BwdIn& in, void* dq, float* dk_
   auto kern = bwd_fused_tc_kernel<D, SETTING>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  const long long blocks = (long long)p.BH * ((p.NQ + BQ - 1) / BQ);
-  kern<<<(unsigned)blocks, THREADS, smem, st>>>(p, in.lse1, in.lse2, in.kl, in.g, static_cast<__nv_bfloat16*>(dq),
-                                                dk_acc, status, mq1, mq2, mk1, mk2);
+  const long long blocks = (long long)p.BH * ((p.NQ + BQ - 1) / BQ - kr.qt_min);
+  kern<<<(unsigned)blocks, THREADS, smem, st>>>(p, kr, in.lse1, in.lse2, in.kl, in.g,
+                                                static_cast<__nv_bfloat16*>(dq), dk_acc, status, mq1, mq2, mk1, mk2);
   return cudaGetLastError();
 }
 
-// dK = scale * acc, rounded to bf16 and written with dK's own strides; acc is
-// the contiguous fp32 [B*H, N_K, D] accumulator.  One thread converts 8 values.
+// out row (row0 + r) of head bh = bf16(scale * acc[bh][r]) for r < nrows, with
+// the output's strides (sb, sh, sn); acc holds acc_rows fp32 rows of D per head.
+// One thread converts 8 values.
 template <int D>
-__global__ void __launch_bounds__(256) acc_convert_kernel(const float4* __restrict__ acc, __nv_bfloat16* __restrict__ out,
-                                                          const Problem p, size_t n8) {
+__global__ void __launch_bounds__(256)
+    acc_convert_kernel(const float4* __restrict__ acc, __nv_bfloat16* __restrict__ out, const int H,
+                       const int acc_rows, const int row0, const int nrows, const long long sb, const long long sh,
+                       const long long sn, const float scale, const size_t n8) {
   for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += (size_t)gridDim.x * blockDim.x) {
-    const float4 a = acc[2 * i], b = acc[2 * i + 1];
-    uint4 o;
-    o.x = pack_bf16(a.x * p.scale, a.y * p.scale);
-    o.y = pack_bf16(a.z * p.scale, a.w * p.scale);
-    o.z = pack_bf16(b.x * p.scale, b.y * p.scale);
-    o.w = pack_bf16(b.z * p.scale, b.w * p.scale);
-    const size_t row = i / (D / 8);
+    const size_t rr = i / (D / 8);
     const int d = (int)(i % (D / 8)) * 8;
-    const int bh = (int)(row / (size_t)p.NK), key = (int)(row % (size_t)p.NK);
-    *reinterpret_cast<uint4*>(out + row_offset(bh, p.H, key, p.ks_b, p.ks_h, p.ks_n) + d) = o;
+    const int bh = (int)(rr / (size_t)nrows), r = (int)(rr % (size_t)nrows);
+    const size_t a = (((size_t)bh * acc_rows + r) * D + d) / 4;
+    const float4 x = acc[a], y = acc[a + 1];
+    uint4 o;
+    o.x = pack_bf16(x.x * scale, x.y * scale);
+    o.y = pack_bf16(x.z * scale, x.w * scale);
+    o.z = pack_bf16(y.x * scale, y.y * scale);
+    o.w = pack_bf16(y.z * scale, y.w * scale);
+    *reinterpret_cast<uint4*>(out + row_offset(bh, H, row0 + r, sb, sh, sn) + d) = o;
   }
 }
 
 template <int D>
-cudaError_t fused_d(const Problem& p, int setting, const BwdIn& in, void* dq, void* dk, float* dk_acc, int* status,
-                    cudaStream_t st) {
-  const size_t n = (size_t)p.BH * p.NK * D;
-  cudaError_t e = cudaMemsetAsync(dk_acc, 0, n * sizeof(float), st);
-  if (e != cudaSuccess) return e;
-  e = setting == 1 ? launch_fused<D, 1>(p, in, dq, dk_acc, status, st)
-                   : launch_fused<D, 2>(p, in, dq, dk_acc, status, st);
-  if (e != cudaSuccess) return e;
-  const size_t n8 = n / 8;
+cudaError_t convert_rows(const float* acc, void* out, const Problem& p, int acc_rows, int row0, int nrows, long long sb,
+                         long long sh, long long sn, cudaStream_t st) {
+  const size_t n8 = (size_t)p.BH * nrows * (D / 8);
+  if (n8 == 0) return cudaSuccess;
   const int blocks = (int)((n8 + 255) / 256 < 4096 ? (n8 + 255) / 256 : 4096);
-  acc_convert_kernel<D><<<blocks > 0 ? blocks : 1, 256, 0, st>>>(reinterpret_cast<const float4*>(dk_acc),
-                                                                 static_cast<__nv_bfloat16*>(dk), p, n8);
+  acc_convert_kernel<D><<<blocks, 256, 0, st>>>(reinterpret_cast<const float4*>(acc),
+                                                static_cast<__nv_bfloat16*>(out), p.H, acc_rows, row0, nrows, sb, sh,
+                                                sn, p.scale, n8);
   return cudaGetLastError();
+}
+
+// First query tile whose rows see key k0 (causal: row i keeps keys j <= i + off).
+int first_qtile(const Problem& p, long long k0) {
+  if (!p.causal) return 0;
+  const long long need = k0 - p.off;  // the tile's last row must reach this
+  if (need <= 0) return 0;
+  return (int)((need + 1 + BQ - 1) / BQ - 1);
+}
+
+template <int D>
+cudaError_t fused_d(const Problem& p, int setting, const BwdIn& in, void* dq, void* dk, float* ws, int range_tiles,
+                    int* status, cudaStream_t st) {
+  const int n_kt = (p.NK + BK - 1) / BK;
+  const int n_ranges = (n_kt + range_tiles - 1) / range_tiles;
+  const int dk_rows = std::min(range_tiles * BK, p.NK);
+  float* dk_acc = ws;
+  float* dq_acc = n_ranges > 1 ? ws + (size_t)p.BH * dk_rows * D : nullptr;
+  for (int r = 0; r < n_ranges; ++r) {
+    const int jt0 = r * range_tiles, jt1 = std::min(n_kt, jt0 + range_tiles);
+    const int k0 = jt0 * BK, nk = std::min(p.NK, jt1 * BK) - k0;
+    cudaError_t e = cudaMemsetAsync(dk_acc, 0, (size_t)p.BH * dk_rows * D * sizeof(float), st);
+    if (e != cudaSuccess) return e;
+    const KeyRange kr{jt0, jt1, first_qtile(p, k0), n_ranges == 1 ? DQ_BF16 : (r == 0 ? DQ_STORE : DQ_ADD), dk_rows,
+                      dq_acc};
+    e = setting == 1 ? launch_fused<D, 1>(p, kr, in, dq, dk_acc, status, st)
+                     : launch_fused<D, 2>(p, kr, in, dq, dk_acc, status, st);
+    if (e != cudaSuccess) return e;
+    e = convert_rows<D>(dk_acc, dk, p, dk_rows, k0, nk, p.ks_b, p.ks_h, p.ks_n, st);
+    if (e != cudaSuccess) return e;
+  }
+  if (n_ranges > 1) return convert_rows<D>(dq_acc, dq, p, p.NQ, 0, p.NQ, p.qs_b, p.qs_h, p.qs_n, st);
+  return cudaSuccess;
 }
 
 }  // namespace
 
-cudaError_t launch_bwd_fused(const Problem& p, int setting, const BwdIn& in, void* dq, void* dk, float* dk_acc,
-                             int* status, cudaStream_t st) {
-  if (p.D == 64) return fused_d<64>(p, setting, in, dq, dk, dk_acc, status, st);
-  return fused_d<128>(p, setting, in, dq, dk, dk_acc, status, st);
+cudaError_t launch_bwd_fused(const Problem& p, int setting, const BwdIn& in, void* dq, void* dk, float* workspace,
+                             int range_tiles, int* status, cudaStream_t st) {
+  if (p.D == 64) return fused_d<64>(p, setting, in, dq, dk, workspace, range_tiles, status, st);
+  return fused_d<128>(p, setting, in, dq, dk, workspace, range_tiles, status, st);
 }
+
+int fused_first_qtile(const Problem& p, long long k0) { return first_qtile(p, k0); }
 
 }  // namespace skl

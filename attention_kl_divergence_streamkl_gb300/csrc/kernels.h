@@ -60,8 +60,14 @@ struct BwdIn {
 // setting 1: dq/dk are dQ2/dK2; setting 2: dQ1/dK1.  The separate path skips a NULL output.
 cudaError_t launch_bwd_separate(const Problem& p, int setting, const BwdIn& in, void* dq, void* dk, int* status,
                                 cudaStream_t st);
-cudaError_t launch_bwd_fused(const Problem& p, int setting, const BwdIn& in, void* dq, void* dk, float* dq_acc,
-                             int* status, cudaStream_t st);
+// Fused backward over key ranges of range_tiles 128-key tiles (all keys when
+// range_tiles >= the tile count).  workspace: the fp32 dK rows of one range
+// ([B*H][min(128 range_tiles, N_K)][D]), then, with more than one range, the
+// fp32 dQ accumulator ([B*H][N_Q][D]).
+cudaError_t launch_bwd_fused(const Problem& p, int setting, const BwdIn& in, void* dq, void* dk, float* workspace,
+                             int range_tiles, int* status, cudaStream_t st);
+// First 128-query tile whose rows see key k0.
+int fused_first_qtile(const Problem& p, long long k0);
 
 // ---- test hook ------------------------------------------------------------------
 cudaError_t launch_wait_timeout_probe(int timeout_us, int* status, cudaStream_t st);

@@ -322,6 +322,7 @@ def run_ours(args):
             ev[3].record(stream)
         return kl, dq, dk
 
+    key_ranges = None
     if decode:
         kernels = ["fwd" if args.nonsplit else "splitk"]
         algo = {kernels[0]: 4 * w.D * pairs}
@@ -333,7 +334,11 @@ def run_ours(args):
     else:
         kernels = ["fwd", "bwd_fused", "none"]
         algo = {"fwd": 4 * w.D * pairs, "bwd_fused": 8 * w.D * pairs}
-        launches_per_step = 3
+        props = torch.cuda.get_device_properties(dev)
+        key_ranges = skl.bwd_fused_plan(w.B, w.H, w.NQ, w.NK, w.D, props.L2_cache_size,
+                                        props.multi_processor_count, w.causal)[0]
+        # fwd; per key range the fused kernel and the dK conversion; the dQ conversion with several ranges
+        launches_per_step = 1 + 2 * key_ranges + (1 if key_ranges > 1 else 0)
 
     for _ in range(args.warmup):
         step((q1, k1, q2, k2))
@@ -458,6 +463,7 @@ def run_ours(args):
             "config": {"workload": w.name, "B": w.B, "H": w.H, "N_Q": w.NQ, "N_K": w.NK, "D": w.D,
                        "causal": w.causal, "setting": args.setting if not decode else None,
                        "layout": args.layout, "bwd_path": None if decode else {1: "fused", 2: "separate"}[mode],
+                       "bwd_key_ranges": key_ranges,
                        "path": ("nonsplit" if args.nonsplit else "splitk") if decode else "fwd+bwd",
                        "per_gpu_units": "the whole workload on every rank (independent heads)",
                        "l2": "inputs larger than L2, no flush between steps",

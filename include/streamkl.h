@@ -77,7 +77,7 @@ typedef struct {
 
 /* Backward path selection (the adaptive rule of section 手法 2 "kernel fusion"). */
 typedef enum {
-  STREAMKL_BWD_AUTO = 0,     /* fused when the live rows of the fp32 dK buffer fit in L2, else separate */
+  STREAMKL_BWD_AUTO = 0,     /* the fused path (over key ranges when N_K is long; see streamkl_bwd_fused_plan) */
   STREAMKL_BWD_FUSED = 1,    /* one pass over each QK tile pair, dQ on chip, dK by atomics into fp32 */
   STREAMKL_BWD_SEPARATE = 2, /* a Q-stationary dQ kernel and a K-stationary dK kernel */
   STREAMKL_BWD_DQ_ONLY = 3,  /* separate path, dQ kernel only (dK pointer may be NULL) */
@@ -143,20 +143,32 @@ streamkl_status streamkl_fwd_splitk_noalloc(const void* q1, const void* k1, cons
                                             float* lse2, void* stream);
 
 /*
- * Backward workspace: fused mode needs an fp32 [B,H,N_K,D] dK accumulator
- * (zeroed by the library; the fused kernel keeps dQ on chip and adds dK
- * partials here); separate mode needs none (0 bytes).  AUTO resolves with the
- * current device's L2 size.
+ * Backward workspace for the current device (0 bytes for the separate path).
+ * The fused path adds dK partials with fp32 atomics into an accumulator that
+ * the library zeroes; they stay cheap while the rows being accumulated sit in
+ * L2.  Its blocks run head by head, so the live rows are one head's keys times
+ * the heads a wave of blocks spans.  When all N_K keys fit that way, one
+ * launch covers them and the workspace is the fp32 [B,H,N_K,D] dK accumulator
+ * (dQ stays on chip).  Otherwise the keys are split into ranges whose live rows
+ * fit in half the L2, each range one launch, and the workspace is the fp32
+ * [B,H,range,D] dK rows of one range followed by an fp32 [B,H,N_Q,D] dQ
+ * accumulator.  streamkl_bwd_fused_plan gives the same figures for any L2
+ * size.  The environment variable STREAMKL_FUSED_KEY_TILES, a positive count of
+ * 128-key tiles, fixes the range length instead (for testing and tuning).
  */
 streamkl_status streamkl_bwd_workspace(streamkl_shape s, int bwd_mode, size_t* bytes);
 /*
- * Which path AUTO takes on a device with `l2_bytes` of L2 and `num_sms` SMs
- * (pure host rule, no device; 0 for an invalid shape).  Fused iff the live part
- * of the fp32 dK buffer fits in L2: the fused blocks run head by head, so that
- * is one head's N_K x D x 4 bytes times the heads a wave of num_sms blocks
- * (128 queries each) spans, plus one.
+ * Which path AUTO takes (pure host rule, no device; 0 for an invalid shape or
+ * num_sms <= 0): the fused path, for every shape.
  */
 int streamkl_bwd_select(streamkl_shape s, size_t l2_bytes, int num_sms);
+/*
+ * The fused path's plan on a device with `l2_bytes` of L2 and `num_sms` SMs
+ * (pure host rule, no device): the number of key ranges (launches) and the
+ * workspace bytes, as described at streamkl_bwd_workspace.
+ */
+streamkl_status streamkl_bwd_fused_plan(streamkl_shape s, size_t l2_bytes, int num_sms, int* key_ranges,
+                                        size_t* workspace_bytes);
 
 /*
  * Setting 1: P1 held fixed, Q2/K2 optimised (standard distillation).

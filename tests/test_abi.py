@@ -96,8 +96,8 @@ def test_bwd_rejects_bad_mode_and_pointers(lib):
     # fused without (enough) workspace is refused before any launch
     assert lib.streamkl_bwd_s1(p[0], p[1], p[2], p[3], s, p[4], p[5], p[6], p[7], p[8], K.BWD_FUSED, None, 0,
                                None) == K.ERR_WORKSPACE
-    assert lib.streamkl_bwd_s1(p[0], p[1], p[2], p[3], s, p[4], p[5], p[6], p[7], p[8], K.BWD_FUSED, p[9],
-                               8 * 64 * 4 - 1, None) == K.ERR_WORKSPACE
+    assert lib.streamkl_bwd_s1(p[0], p[1], p[2], p[3], s, p[4], p[5], p[6], p[7], p[8], K.BWD_FUSED, fake_ptr(8),
+                               1 << 20, None) == K.ERR_WORKSPACE  # misaligned workspace
 
 
 def test_workspace_sizes(lib):
@@ -107,9 +107,7 @@ def test_workspace_sizes(lib):
     assert n.value == 8 * 32 * 4 * 19 * 5 * 4
     s16 = K.make_shape(8, 32, 17, 131072, 128)
     assert lib.streamkl_fwd_splitk_workspace(s16, 19, ctypes.byref(n)) == K.ERR_UNSUPPORTED
-    s = K.make_shape(2, 32, 4096, 8192, 128)  # fused: fp32 dK accumulator [B, H, N_K, D]
-    assert lib.streamkl_bwd_workspace(s, K.BWD_FUSED, ctypes.byref(n)) == K.OK
-    assert n.value == 2 * 32 * 8192 * 128 * 4
+    s = K.make_shape(2, 32, 4096, 8192, 128)
     assert lib.streamkl_bwd_workspace(s, K.BWD_SEPARATE, ctypes.byref(n)) == K.OK
     assert n.value == 0
     for mode in (K.BWD_DQ_ONLY, K.BWD_DK_ONLY):
@@ -155,22 +153,57 @@ def _live_rows_bytes(B, H, NQ, NK, D, sms):
     return NK * D * 4 * heads
 
 
-def test_bwd_select_rule(lib):
-    # fused exactly while the live dK rows (heads in flight x N_K x D x 4 B) fit in L2
+def _first_qtile(NQ, NK, k0, causal):
+    need = k0 - (NK - NQ)
+    return 0 if (not causal or need <= 0) else -(-(need + 1) // 128) - 1
+
+
+def _fused_plan(B, H, NQ, NK, D, l2, sms, causal):
+    """The fused backward's key-range rule, restated: every key at once while the live dK rows fit in L2, else
+    the longest range whose live rows (counted with the last range's query tiles) fit in half of it."""
+    n_kt, n_qt = -(-NK // 128), -(-NQ // 128)
+    if _live_rows_bytes(B, H, NQ, NK, D, sms) <= l2:
+        return 1, B * H * NK * D * 4
+    n = 2
+    while True:
+        tiles = -(-n_kt // n)
+        ranges = -(-n_kt // tiles)
+        qtiles = max(1, n_qt - _first_qtile(NQ, NK, (ranges - 1) * tiles * 128, causal))
+        heads = min(B * H, -(-sms // qtiles) + 1)
+        if tiles <= 1 or min(tiles * 128, NK) * D * 4 * heads <= l2 // 2:
+            break
+        n += 1
+    ranges = -(-n_kt // tiles)
+    return ranges, B * H * min(tiles * 128, NK) * D * 4 + (B * H * NQ * D * 4 if ranges > 1 else 0)
+
+
+def test_bwd_select_and_fused_plan(lib):
     l2, sms = 135528448, 152  # GB300
-    assert K.bwd_select(1, 1, 128, 128, 64, l2, sms) == K.BWD_FUSED
-    assert K.bwd_select(2, 32, 4096, 4096, 128, l2, sms) == K.BWD_FUSED  # whole buffer 128 MiB; live 12 MiB
-    assert K.bwd_select(1, 32, 65536, 65536, 128, l2, sms) == K.BWD_FUSED  # live: 2 heads x 32 MiB
-    assert K.bwd_select(1, 8, 524288, 524288, 128, l2, sms) == K.BWD_SEPARATE  # one head's rows: 256 MiB
-    for n in (100000, 120000, 131072, 140000, 200000):
-        want = K.BWD_FUSED if _live_rows_bytes(1, 8, n, n, 128, sms) <= l2 else K.BWD_SEPARATE
-        assert K.bwd_select(1, 8, n, n, 128, l2, sms) == want, n
-    # few query tiles: a wave spans many heads, all of whose rows are live
-    assert _live_rows_bytes(64, 32, 256, 4096, 128, sms) == 4096 * 128 * 4 * 77
-    assert K.bwd_select(64, 32, 256, 4096, 128, 77 * 4096 * 512, sms) == K.BWD_FUSED
-    assert K.bwd_select(64, 32, 256, 4096, 128, 77 * 4096 * 512 - 1, sms) == K.BWD_SEPARATE
+    assert K.bwd_select(1, 8, 524288, 524288, 128, l2, sms) == K.BWD_FUSED  # AUTO is always the fused path
     assert K.bwd_select(0, 1, 8, 8, 64, l2, sms) == 0  # invalid shape
     assert K.bwd_select(1, 1, 8, 8, 64, l2, 0) == 0  # no SM count
+    # one launch while the live dK rows (heads in flight x N_K x D x 4 B) fit in L2
+    assert K.bwd_fused_plan(1, 1, 128, 128, 64, l2, sms, False) == (1, 128 * 64 * 4)
+    assert K.bwd_fused_plan(2, 32, 4096, 8192, 128, l2, sms, False) == (1, 2 * 32 * 8192 * 128 * 4)
+    assert K.bwd_fused_plan(1, 32, 65536, 65536, 128, l2, sms, True) == (1, 32 * 65536 * 128 * 4)  # live 64 MiB
+    # the 512K workload: one head's rows alone are 256 MiB -> 8 ranges of 64K keys (2 heads x 32 MiB live),
+    # workspace = one range's dK rows + the fp32 dQ accumulator
+    assert K.bwd_fused_plan(1, 8, 524288, 524288, 128, l2, sms, True) == (8, 8 * 65536 * 512 + 8 * 524288 * 512)
+    for B, H, NQ, NK, causal in [(1, 8, 100000, 100000, True), (1, 8, 131072, 131072, False), (1, 4, 1000, 200000, True),
+                                 (1, 8, 140000, 140000, True), (64, 32, 256, 4096, False), (1, 8, 200000, 260000, True)]:
+        for l2b in (l2, l2 // 8, 77 * 4096 * 512, 77 * 4096 * 512 - 1):
+            assert K.bwd_fused_plan(B, H, NQ, NK, 128, l2b, sms, causal) == _fused_plan(B, H, NQ, NK, 128, l2b, sms,
+                                                                                      causal), (B, H, NQ, NK, l2b)
+
+
+def test_fused_range_override(lib, monkeypatch):
+    l2, sms = 135528448, 152
+    monkeypatch.setenv("STREAMKL_FUSED_KEY_TILES", "2")
+    assert K.bwd_fused_plan(2, 3, 300, 1000, 64, l2, sms, True) == (4, 2 * 3 * 256 * 64 * 4 + 2 * 3 * 300 * 64 * 4)
+    monkeypatch.setenv("STREAMKL_FUSED_KEY_TILES", "100")  # longer than N_K: one launch
+    assert K.bwd_fused_plan(2, 3, 300, 1000, 64, l2, sms, True) == (1, 2 * 3 * 1000 * 64 * 4)
+    monkeypatch.setenv("STREAMKL_FUSED_KEY_TILES", "0")  # not positive: ignored
+    assert K.bwd_fused_plan(2, 3, 300, 1000, 64, l2, sms, True) == (1, 2 * 3 * 1000 * 64 * 4)
 
 
 @pytest.mark.parametrize("qs,ks,code", [

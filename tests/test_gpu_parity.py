@@ -176,23 +176,29 @@ def test_decode_splitk(nq):
 
 
 def test_b1h8_n524288_causal_setting2():
-    """The 512K causal workload: fwd + setting 2 on the separate path; 128 sampled rows, dK1 invariants."""
+    """The 512K causal workload: fwd + setting 2, on the fused path over key ranges (what AUTO takes: one head's
+    dK rows, 256 MiB, exceed L2) and on the separate path; 128 sampled rows each, and the dK1 invariants."""
     w = W["kl_b1h8_n524288_d128_causal"]
     inp = synth.make_inputs(w)
     kl, l1, l2 = _run_fwd(inp, w)
     props = torch.cuda.get_device_properties(0)
     assert skl.bwd_select(w.B, w.H, w.NQ, w.NK, w.D, props.L2_cache_size, props.multi_processor_count,
-                          w.causal) == skl.BWD_SEPARATE
-    dq, dk = _run_bwd(inp, w, 2, skl.BWD_AUTO, kl, l1, l2)
-    torch.cuda.synchronize()
+                          w.causal) == skl.BWD_FUSED
+    ranges, _ = skl.bwd_fused_plan(w.B, w.H, w.NQ, w.NK, w.D, props.L2_cache_size, props.multi_processor_count,
+                                   w.causal)
+    assert ranges > 1
     rows = synth.sample_rows(w, 128, 1000 + w.seed)
     rkl, rl1, rl2, rdq = U.oracle_rows(inp, w, rows, setting=2)
     b, h, i = rows[:, 0], rows[:, 1], rows[:, 2]
     U.assert_rows(U.np64(kl)[b, h, i], U.np64(l1)[b, h, i], U.np64(l2)[b, h, i], rkl, rl1, rl2)
-    U.assert_grad(U.np64(dq)[b, h, i], rdq, "dQ1 sampled rows")
     q1, k1, q2, k2 = U.dev_inputs(inp)
-    r_sum, r_tr = U.dk_invariants(dk, k1, dq, q1)
-    assert r_sum < 2e-2 and r_tr < 2e-2, (r_sum, r_tr)
+    for mode in (skl.BWD_AUTO, skl.BWD_SEPARATE):
+        dq, dk = _run_bwd(inp, w, 2, mode, kl, l1, l2)
+        torch.cuda.synchronize()
+        U.assert_grad(U.np64(dq)[b, h, i], rdq, f"mode {mode}: dQ1 sampled rows")
+        r_sum, r_tr = U.dk_invariants(dk, k1, dq, q1)
+        assert r_sum < 2e-2 and r_tr < 2e-2, (mode, r_sum, r_tr)
+        del dq, dk
 
 
 # ------------------------------------------------------------------ edge cases
@@ -244,6 +250,23 @@ def test_workspace_too_small_is_refused():
     st = skl.lib().streamkl_fwd_splitk(*(ctypes.c_void_p(t.data_ptr()) for t in (q1, k1, q2, k2)), s, 4,
                                        ctypes.c_void_p(ws.data_ptr()), 16,
                                        *(ctypes.c_void_p(t.data_ptr()) for t in out), None)
+    assert st == skl._lib.ERR_WORKSPACE
+
+
+def test_fused_workspace_too_small_is_refused():
+    w = synth.Workload("ws", 1, 2, 100, 300, 64, True, 0.5, 11)
+    inp = synth.make_inputs(w)
+    q1, k1, q2, k2 = U.dev_inputs(inp)
+    import ctypes
+    s = skl.make_shape(1, 2, 100, 300, 64, w.softmax_scale, True)
+    need = skl.bwd_workspace_bytes(1, 2, 100, 300, 64, skl.BWD_FUSED, True)
+    assert need == 2 * 300 * 64 * 4
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    rows = [torch.zeros((1, 2, 100), device="cuda") for _ in range(3)]
+    dq, dk = torch.empty_like(q2), torch.empty_like(k2)
+    ptr = lambda t: ctypes.c_void_p(t.data_ptr())  # noqa: E731
+    st = skl.lib().streamkl_bwd_s1(*(ptr(t) for t in (q1, k1, q2, k2)), s, *(ptr(t) for t in rows), ptr(dq), ptr(dk),
+                                   skl.BWD_FUSED, ptr(ws), need - 1, None)
     assert st == skl._lib.ERR_WORKSPACE
 
 
