@@ -3,8 +3,10 @@
 // StreamKL technical summary (gist.science/ja/paper/2606.20005), section 手法 2
 // "kernel fusion": each (query tile, key tile) pair is visited exactly once.
 // Here the query tile is stationary: dQ accumulates in TMEM along the keys, and
-// the dK partial of each key tile is added into an fp32 buffer with atomics --
-// the path the library takes while that buffer fits in L2.  dS arithmetic in
+// the dK partial of each key tile is added into an fp32 buffer with atomics,
+// which stay cheap while the rows being accumulated sit in L2.  For long key
+// sequences the host runs the kernel once per key range sized to keep them
+// there, summing dQ over the ranges in fp32 (KeyRange below).  dS arithmetic in
 // ds_math.cuh (setting 1: dS2 = g (P2 - P1); setting 2: dS1 = g P1 (r - KL)).
 //
 // Block = one 128-query tile (stationary Q1, Q2 in smem; queries on the 128 TMEM
