@@ -14,8 +14,12 @@
 //     acc += sum_j 2^(x1_j - m1) (q1.k1_j - q2.k2_j)
 //     m2, l2 likewise from x2
 // The maximum is only moved when it grows by more than 2^8 (terms stay <= 256,
-// far from fp32 overflow); this is exact because l1 and acc share m1.  At the
-// end LSE_t = ln2 (m_t + log2 l_t) and KL = scale acc / l1 + LSE2 - LSE1.
+// far from fp32 overflow); this is exact because l1 and acc share m1.  Once a
+// row has finite maxima, a tile is first summed against them without taking its
+// own maximum: if every term stays below 2^64 (the tile's sums show it, inf
+// included) the sums are kept, else the tile is redone with its maximum as
+// above.  At the end LSE_t = ln2 (m_t + log2 l_t) and KL = scale acc / l1 +
+// LSE2 - LSE1.
 //
 // Block layout (one 128-row query tile per block, key tiles of 128):
 //   warp 8      TMA producer: Q1, Q2 once, then K1/K2 tiles through 2 stages
@@ -41,6 +45,7 @@ constexpr int PRODUCER_WARP = 8;
 constexpr int MMA_WARP = 9;
 constexpr int THREADS = 10 * 32;
 constexpr float kLazy = 8.0f;
+constexpr float kFastSumLimit = 18446744073709551616.0f;  // 2^64
 constexpr uint32_t kTmemCols = 512;
 constexpr int kOneBlockPerSmSmem = 120 * 1024;
 
@@ -84,6 +89,39 @@ __device__ __forceinline__ void online_update(Row5& st, uint32_t (&a0)[32], uint
       }
     }
   }
+  const float2 cc = make_float2(c, c);
+  // sums of 2^(c s - m) over the 64 columns against the maxima m1, m2
+  auto tile_sums = [&](float m1, float m2, float2& l1, float2& l2, float2& acc) {
+    const float2 n1 = make_float2(-m1, -m1), n2 = make_float2(-m2, -m2);
+    l1 = l2 = acc = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+#pragma unroll
+      for (int i = 0; i < 32; i += 2) {
+        const uint32_t* A = h == 0 ? a0 : a1;
+        const uint32_t* Bv = h == 0 ? b0 : b1;
+        const float2 s1 = make_float2(__uint_as_float(A[i]), __uint_as_float(A[i + 1]));
+        const float2 s2 = make_float2(__uint_as_float(Bv[i]), __uint_as_float(Bv[i + 1]));
+        const float2 x1 = ffma2(s1, cc, n1), x2 = ffma2(s2, cc, n2);
+        const float2 p1 = make_float2(ex2(x1.x), ex2(x1.y));
+        const float2 p2 = make_float2(ex2(x2.x), ex2(x2.y));
+        l1 = fadd2(l1, p1);
+        l2 = fadd2(l2, p2);
+        acc = ffma2(p1, fsub2(s1, s2), acc);
+      }
+    }
+  };
+  float2 l1, l2, acc;
+  if (st.m1 != kNegInf && st.m2 != kNegInf) {
+    tile_sums(st.m1, st.m2, l1, l2, acc);
+    const float t1 = l1.x + l1.y, t2 = l2.x + l2.y;
+    if (t1 < kFastSumLimit && t2 < kFastSumLimit) {  // false for inf and NaN too
+      st.l1 += t1;
+      st.l2 += t2;
+      st.acc += acc.x + acc.y;
+      return;
+    }
+  }
   float mx1 = kMaskedLogit, mx2 = kMaskedLogit;
 #pragma unroll
   for (int i = 0; i < 32; ++i) {
@@ -103,25 +141,7 @@ __device__ __forceinline__ void online_update(Row5& st, uint32_t (&a0)[32], uint
     st.l2 *= al;
     st.m2 = t2;
   }
-  const float2 cc = make_float2(c, c);
-  const float2 n1 = make_float2(-st.m1, -st.m1), n2 = make_float2(-st.m2, -st.m2);
-  float2 l1 = make_float2(0.f, 0.f), l2 = make_float2(0.f, 0.f), acc = make_float2(0.f, 0.f);
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-#pragma unroll
-    for (int i = 0; i < 32; i += 2) {
-      const uint32_t* A = h == 0 ? a0 : a1;
-      const uint32_t* Bv = h == 0 ? b0 : b1;
-      const float2 s1 = make_float2(__uint_as_float(A[i]), __uint_as_float(A[i + 1]));
-      const float2 s2 = make_float2(__uint_as_float(Bv[i]), __uint_as_float(Bv[i + 1]));
-      const float2 x1 = ffma2(s1, cc, n1), x2 = ffma2(s2, cc, n2);
-      const float2 p1 = make_float2(ex2(x1.x), ex2(x1.y));
-      const float2 p2 = make_float2(ex2(x2.x), ex2(x2.y));
-      l1 = fadd2(l1, p1);
-      l2 = fadd2(l2, p2);
-      acc = ffma2(p1, fsub2(s1, s2), acc);
-    }
-  }
+  tile_sums(st.m1, st.m2, l1, l2, acc);
   st.l1 += l1.x + l1.y;
   st.l2 += l2.x + l2.y;
   st.acc += acc.x + acc.y;

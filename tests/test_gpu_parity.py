@@ -203,6 +203,24 @@ def test_b1h8_n524288_causal_setting2():
 
 # ------------------------------------------------------------------ edge cases
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_logits_growing_past_the_first_tile(causal):
+    """Keys after the first tile scaled by 30: the row maxima jump by far more than 2^64 (log2 units) after the
+    first tile, so the forward's tiles that reuse the running maxima must detect it and redo the tile against
+    its own maximum."""
+    w = synth.Workload("growth", 1, 2, 256, 512, 64, causal, 0.5, 21)
+    inp = synth.make_inputs(w)
+    for k in ("k1", "k2"):
+        f = U.f64(inp[k])
+        f[:, :, 128:] *= 30.0
+        inp[k] = synth.f32_to_bf16_bits(f.astype(np.float32))
+    Q1, K1, Q2, K2 = (U.f64(inp[k]) for k in ("q1", "k1", "q2", "k2"))
+    rkl, rl1, rl2 = O.forward(Q1, K1, Q2, K2, w.softmax_scale, causal)
+    assert (rl1[:, :, 200:] * np.log2(np.e) - 64).max() > 0  # the late rows' maxima are far above the first tile's
+    kl, l1, l2 = _run_fwd(inp, w)
+    U.assert_rows(U.np64(kl), U.np64(l1), U.np64(l2), rkl, rl1, rl2, "growth fwd")
+
+
 def test_identical_pairs_give_exact_zero():
     w = synth.Workload("same", 1, 2, 200, 200, 128, True, 0.5, 7)
     inp = synth.make_inputs(w)
