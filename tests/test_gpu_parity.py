@@ -221,6 +221,25 @@ def test_logits_growing_past_the_first_tile(causal):
     U.assert_rows(U.np64(kl), U.np64(l1), U.np64(l2), rkl, rl1, rl2, "growth fwd")
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_upstream_gradient_of_mixed_sign(causal):
+    """g of either sign and zero rows: the fused path folds a positive g into its exponents and multiplies by
+    any other g; both settings and both paths against the oracle."""
+    w = synth.Workload("gsign", 2, 2, 300, 300, 128, causal, 0.5, 23)
+    inp = synth.make_inputs(w)
+    g = (np.random.default_rng(5).standard_normal((2, 2, 300)) / 300).astype(np.float32)
+    g[:, :, ::7] = 0.0
+    inp["g"] = g
+    kl, l1, l2 = _run_fwd(inp, w)
+    Q1, K1, Q2, K2 = (U.f64(inp[k]) for k in ("q1", "k1", "q2", "k2"))
+    for setting in (1, 2):
+        rdq, rdk = O.backward(setting, Q1, K1, Q2, K2, w.softmax_scale, causal, g)
+        for mode in (skl.BWD_FUSED, skl.BWD_SEPARATE):
+            dq, dk = _run_bwd(inp, w, setting, mode, kl, l1, l2)
+            U.assert_grad(U.np64(dq), rdq, f"setting {setting} mode {mode} dQ")
+            U.assert_grad(U.np64(dk), rdk, f"setting {setting} mode {mode} dK")
+
+
 def test_identical_pairs_give_exact_zero():
     w = synth.Workload("same", 1, 2, 200, 200, 128, True, 0.5, 7)
     inp = synth.make_inputs(w)
