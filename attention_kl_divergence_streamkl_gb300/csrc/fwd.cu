@@ -159,9 +159,11 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t sb = smem_u32(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_qt = (p.NQ + BM - 1) / BM;
-  const int bh = blockIdx.x % p.BH;
+  // heads in order, so the blocks in flight share one head's K tiles in L2; within a head the longest
+  // causal tiles first
+  const int bh = (int)(blockIdx.x / n_qt);
   const int mh = bh % p.H, mb = bh / p.H;  // head and batch coordinates of the tensor maps
-  const int qt = n_qt - 1 - (int)(blockIdx.x / p.BH);  // longest causal tiles first
+  const int qt = n_qt - 1 - (int)(blockIdx.x % n_qt);
   const int q0 = qt * BM;
   const int q_last = min(p.NQ, q0 + BM) - 1;
   const int kend = p.causal ? min(p.NK, q_last + p.off + 1) : p.NK;
