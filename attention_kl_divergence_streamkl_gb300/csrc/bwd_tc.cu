@@ -85,9 +85,11 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int NX = p.NQ, NY = p.NK;
   const int n_xt = (NX + BX - 1) / BX;
-  const int bh = blockIdx.x % p.BH;
+  // heads in order (the blocks in flight share one head's K tiles in L2), longest blocks (the last query
+  // tiles) first within a head
+  const int bh = (int)(blockIdx.x / n_xt);
   const int mh = bh % p.H, mb = bh / p.H;  // head and batch coordinates of the tensor maps
-  const int xt = n_xt - 1 - (int)(blockIdx.x / p.BH);  // longest blocks (the last query tiles) first
+  const int xt = n_xt - 1 - (int)(blockIdx.x % n_xt);
   const int x0 = xt * BX;
   const int y_end = p.causal ? min(NY, min(NX, x0 + BX) - 1 + p.off + 1) : NY;  // keys the last row sees
   const int n_yt = (y_end + BY - 1) / BY;
@@ -361,9 +363,12 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint8_t* smem = align1024(smem_raw);
   const uint32_t sb = smem_u32(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int bh = blockIdx.x % p.BH;
+  // heads in order (the blocks in flight share one head's Q tiles in L2); within a head the first key
+  // tiles, which see the most queries, first
+  const int n_kt_all = (p.NK + BK - 1) / BK;
+  const int bh = (int)(blockIdx.x / n_kt_all);
   const int mh = bh % p.H, mb = bh / p.H;  // head and batch coordinates of the tensor maps
-  const int kt = (int)(blockIdx.x / p.BH);  // longest first: the first key tiles see the most queries
+  const int kt = (int)(blockIdx.x % n_kt_all);
   const int k0 = kt * BK;
   const int q_begin = p.causal ? max(0, k0 - p.off) / BQ * BQ : 0;
   const int n_qt = (p.NQ - q_begin + BQ - 1) / BQ;
