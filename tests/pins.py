@@ -195,3 +195,46 @@ def check_online_identity(seed=4, d=8, scale=0.8):
 
 ALL_CHECKS = (check_finite_differences, check_torch_library, check_closed_forms, check_invariants,
               check_online_identity)
+
+
+def check_batched_wrappers(seed=5, B=2, H=3, d=8, scale=0.45, tol=1e-10):
+    """The [B, H] entry points forward / backward against torch CPU float64 on the whole batch at once.
+
+    torch's log_softmax, kl_div and autograd run over [B, H, N_Q, N_K] logits,
+    so a head or batch index taken from the wrong place in the oracle's loops
+    (inputs, g, or where a result is stored) shows up as a mismatch.  Masked
+    logits are set to -1e4, whose exp underflows to exactly 0 in float64, so
+    masked keys carry no weight and no NaN enters the gradient.
+    """
+    import torch
+    fails = []
+    rng = np.random.default_rng(seed)
+    for nq, nk, causal in ((6, 6, True), (5, 9, False), (4, 10, True)):
+        arr = [_rand(rng, B, H, nq, d), _rand(rng, B, H, nk, d), _rand(rng, B, H, nq, d), _rand(rng, B, H, nk, d)]
+        g = rng.uniform(0.2, 2.0, (B, H, nq)) * (1.0 + np.arange(B * H).reshape(B, H, 1))
+        kl, l1, l2 = O.forward(*arr, scale, causal, block=4)
+        keep = torch.ones(nq, nk, dtype=torch.bool)
+        if causal:
+            keep = torch.arange(nk)[None, :] <= torch.arange(nq)[:, None] + (nk - nq)
+        for setting in (1, 2):
+            t = [torch.tensor(a, dtype=torch.float64, requires_grad=True) for a in arr]
+            S1 = (scale * t[0] @ t[1].transpose(-1, -2)).masked_fill(~keep, -1e4)
+            S2 = (scale * t[2] @ t[3].transpose(-1, -2)).masked_fill(~keep, -1e4)
+            lp1, lp2 = torch.log_softmax(S1, dim=-1), torch.log_softmax(S2, dim=-1)
+            rows_kl = torch.nn.functional.kl_div(lp2, lp1, reduction="none", log_target=True).sum(dim=-1)
+            (torch.tensor(g) * rows_kl).sum().backward()
+            for name, got, ref in (("KL", kl, rows_kl), ("LSE1", l1, torch.logsumexp(S1, -1)),
+                                   ("LSE2", l2, torch.logsumexp(S2, -1))):
+                e = np.max(np.abs(np.asarray(got) - ref.detach().numpy()))
+                if not e < tol:
+                    fails.append(f"batched {name} nq={nq} nk={nk} causal={causal}: max err {e:.3e}")
+            dq, dk = O.backward(setting, *arr, scale, causal, g, block=3)
+            tq, tk = (t[2], t[3]) if setting == 1 else (t[0], t[1])
+            for name, got, ref in (("dQ", dq, tq.grad.numpy()), ("dK", dk, tk.grad.numpy())):
+                e = np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-300)
+                if not e < tol:
+                    fails.append(f"batched setting {setting} {name} nq={nq} nk={nk} causal={causal}: rel {e:.3e}")
+    return fails
+
+
+ALL_CHECKS = ALL_CHECKS + (check_batched_wrappers,)

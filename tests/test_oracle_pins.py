@@ -168,9 +168,32 @@ def _mut_transposed_dk(mp):
     mp.setattr(O, "head_backward", bad)
 
 
+def _mut_wrapper_g_of_next_head(mp):
+    orig = O.head_backward
+
+    def bad(setting, Q1, K1, Q2, K2, scale, causal, g, block=O.ROW_BLOCK):
+        B, H, nq, d = Q1.shape
+        dq, dk = np.empty((B, H, nq, d)), np.empty((B, H, K1.shape[2], d))
+        for b in range(B):
+            for h in range(H):
+                dq[b, h], dk[b, h] = orig(setting, Q1[b, h], K1[b, h], Q2[b, h], K2[b, h], scale, causal,
+                                          g[b, (h + 1) % H], block)
+        return dq, dk
+    mp.setattr(O, "backward", bad)
+
+
+def _mut_wrapper_batch_heads_swapped(mp):
+    orig = O.forward
+
+    def bad(Q1, K1, Q2, K2, scale, causal, block=O.ROW_BLOCK):
+        return tuple(x[::-1].copy() for x in orig(Q1, K1, Q2, K2, scale, causal, block))
+    mp.setattr(O, "forward", bad)
+
+
 @pytest.mark.parametrize("mutation", [_mut_reverse_kl, _mut_flip_ds2, _mut_drop_kl_term, _mut_drop_scale_dq,
                                       _mut_mask_off_by_one, _mut_lse_without_max, _mut_g_on_keys,
-                                      _mut_transposed_dk], ids=lambda f: f.__name__[5:])
+                                      _mut_transposed_dk, _mut_wrapper_g_of_next_head,
+                                      _mut_wrapper_batch_heads_swapped], ids=lambda f: f.__name__[5:])
 def test_planted_mistake_is_caught(monkeypatch, mutation):
     mutation(monkeypatch)
     assert _run_all(), "a planted mistake passed every pin"
