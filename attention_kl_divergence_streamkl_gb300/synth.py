@@ -123,6 +123,17 @@ def head_slice(w: Workload, which: str, b: int, h: int) -> np.ndarray:
     return f32_to_bf16_bits(student)
 
 
+def head_rows(w: Workload, which: str, b: int, h: int, n: int) -> np.ndarray:
+    """The first ``n`` rows of ``head_slice(w, which, b, h)`` without drawing the rest.
+
+    Each Philox stream fills its ``[N, D]`` array row by row, so a shorter draw
+    is a prefix of the full one.
+    """
+    is_q = which[0] == "q"
+    full = w.NQ if is_q else w.NK
+    return head_slice(w.with_(**({"NQ": min(n, full)} if is_q else {"NK": min(n, full)})), which, b, h)
+
+
 def _threads() -> int:
     try:
         return max(1, min(32, len(os.sched_getaffinity(0))))

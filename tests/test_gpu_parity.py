@@ -74,10 +74,13 @@ def test_small_shapes_full_oracle(case):
         U.assert_rows(*(U.np64(x) for x in skl_), rkl, rl1, rl2, "splitk")
     for setting in (1, 2):
         rdq, rdk = O.backward(setting, Q1, K1, Q2, K2, w.softmax_scale, causal, inp["g"])
+        Qo, Ko = (Q2, K2) if setting == 1 else (Q1, K1)
+        zq = U.zero_grad_tol(inp["g"], w.softmax_scale, Ko)
+        zk = U.zero_grad_tol(np.abs(inp["g"]).sum(axis=-1), w.softmax_scale, Qo)
         for mode in (skl.BWD_FUSED, skl.BWD_SEPARATE):
             dq, dk = _run_bwd(inp, w, setting, mode, kl, l1, l2)
-            U.assert_grad(U.np64(dq), rdq, f"setting {setting} mode {mode} dQ")
-            U.assert_grad(U.np64(dk), rdk, f"setting {setting} mode {mode} dK")
+            U.assert_grad(U.np64(dq), rdq, f"setting {setting} mode {mode} dQ", zero_tol=zq)
+            U.assert_grad(U.np64(dk), rdk, f"setting {setting} mode {mode} dK", zero_tol=zk)
 
 
 def test_128_row_workload_fwd_and_setting1():
@@ -97,34 +100,41 @@ def test_128_row_workload_fwd_and_setting1():
 
 @pytest.mark.parametrize("name", ["kl_b2h32_n4096_d128", "kl_b2h32_n4096_d128_causal"])
 def test_b2h32_n4096(name):
-    """Both settings, both backward paths; full oracle on two seeded heads, invariants on all."""
+    """KL/LSE of every row of every head against the full oracle; both settings and both backward paths
+    against the full oracle on 8 seeded heads; fused = separate and the dK identities on every head."""
     w = W[name]
     inp = synth.make_inputs(w)
     kl, l1, l2 = _run_fwd(inp, w)
+    torch.cuda.synchronize()
+    every = [(b, h) for b in range(w.B) for h in range(w.H)]
+    rkl, rl1, rl2 = U.oracle_forward_heads(inp, w, every)
+    U.assert_rows(U.np64(kl).reshape(-1, w.NQ), U.np64(l1).reshape(-1, w.NQ), U.np64(l2).reshape(-1, w.NQ),
+                  rkl, rl1, rl2, "every row")
     rng = np.random.default_rng(1000 + w.seed)
-    heads = [(int(rng.integers(w.B)), int(rng.integers(w.H))) for _ in range(2)]
+    picks = rng.choice(len(every), size=8, replace=False)
+    heads = [every[int(x)] for x in sorted(picks)]
     q1, k1, q2, k2 = U.dev_inputs(inp)
     for setting in (1, 2):
         outs = {m: _run_bwd(inp, w, setting, m, kl, l1, l2) for m in (skl.BWD_FUSED, skl.BWD_SEPARATE)}
-        for (b, h) in heads:
-            (rkl, rl1, rl2), (rdq, rdk) = U.oracle_head(inp, w, b, h, setting=setting)
-            U.assert_rows(U.np64(kl[b, h]), U.np64(l1[b, h]), U.np64(l2[b, h]), rkl, rl1, rl2, f"head {b},{h}")
+        torch.cuda.synchronize()
+        refs = U.map_heads(lambda b, h: U.oracle_head(inp, w, b, h, setting=setting)[1], heads)
+        for (b, h), (rdq, rdk) in zip(heads, refs):
             for m, (dq, dk) in outs.items():
                 U.assert_grad(U.np64(dq[b, h]), rdq, f"setting {setting} mode {m} dQ head {b},{h}")
                 U.assert_grad(U.np64(dk[b, h]), rdk, f"setting {setting} mode {m} dK head {b},{h}")
         # fused = separate on every head (separate is deterministic and checked above)
         for which in (0, 1):
             f, s_ = outs[skl.BWD_FUSED][which].double(), outs[skl.BWD_SEPARATE][which].double()
-            per_head = ((f - s_).norm(dim=(2, 3)) / s_.norm(dim=(2, 3)).clamp_min(1e-30)).max().item()
+            per_head = ((f - s_).norm(dim=(2, 3)) / s_.norm(dim=(2, 3))).max().item()
             assert per_head < 1e-2, ("dQ" if which == 0 else "dK", per_head)
         qo, ko = (q2, k2) if setting == 1 else (q1, k1)
         for m, (dq, dk) in outs.items():
-            r_sum, r_tr = U.dk_invariants(dk, ko, dq, qo)
-            assert r_sum < 1e-2 and r_tr < 1e-2, (m, r_sum, r_tr)
+            U.assert_dk_invariants(dk, ko, dq, qo, setting, f"setting {setting} mode {m}")
 
 
 def test_b1h32_n65536_causal_setting1():
-    """The long causal workload: 256 sampled rows (KL, LSE, dQ2) and dK2 invariants."""
+    """The long causal workload: 256 sampled rows (KL, LSE, dQ2); dK2 of the last 256 keys of 4 seeded heads
+    against the oracle (only the last 256 query rows see them); the dK2 identities on every head."""
     w = W["kl_b1h32_n65536_d128_causal"]
     inp = synth.make_inputs(w)
     kl, l1, l2 = _run_fwd(inp, w)
@@ -135,9 +145,14 @@ def test_b1h32_n65536_causal_setting1():
     b, h, i = rows[:, 0], rows[:, 1], rows[:, 2]
     U.assert_rows(U.np64(kl)[b, h, i], U.np64(l1)[b, h, i], U.np64(l2)[b, h, i], rkl, rl1, rl2)
     U.assert_grad(U.np64(dq)[b, h, i], rdq, "dQ2 sampled rows")
+    R = 256
+    rng = np.random.default_rng(3000 + w.seed)
+    heads = [(0, int(x)) for x in sorted(rng.choice(w.H, size=4, replace=False))]
+    refs = U.map_heads(lambda bb, hh: U.oracle_last_keys_dk(inp, w, bb, hh, 1, R), heads, threads=4)
+    for (bb, hh), rdk in zip(heads, refs):
+        U.assert_grad(U.np64(dk[bb, hh, -R:]), rdk, f"dK2 last {R} keys head {bb},{hh}")
     q1, k1, q2, k2 = U.dev_inputs(inp)
-    r_sum, r_tr = U.dk_invariants(dk, k2, dq, q2)
-    assert r_sum < 2e-2 and r_tr < 2e-2, (r_sum, r_tr)
+    U.assert_dk_invariants(dk, k2, dq, q2, 1, "dK2")
 
 
 @pytest.mark.slow
@@ -177,7 +192,9 @@ def test_decode_splitk(nq):
 
 def test_b1h8_n524288_causal_setting2():
     """The 512K causal workload: fwd + setting 2, on the fused path over key ranges (what AUTO takes: one head's
-    dK rows, 256 MiB, exceed L2) and on the separate path; 128 sampled rows each, and the dK1 invariants."""
+    dK rows, 256 MiB, exceed L2) and on the separate path.  128 sampled rows (KL, LSE, dQ1); dK1 of the last 128
+    keys of every head against the oracle (only the last 128 query rows see them; they lie in the last key
+    range); sum_j dK_j = 0 and the trace identity on every head."""
     w = W["kl_b1h8_n524288_d128_causal"]
     inp = synth.make_inputs(w)
     kl, l1, l2 = _run_fwd(inp, w)
@@ -191,13 +208,17 @@ def test_b1h8_n524288_causal_setting2():
     rkl, rl1, rl2, rdq = U.oracle_rows(inp, w, rows, setting=2)
     b, h, i = rows[:, 0], rows[:, 1], rows[:, 2]
     U.assert_rows(U.np64(kl)[b, h, i], U.np64(l1)[b, h, i], U.np64(l2)[b, h, i], rkl, rl1, rl2)
+    R = 128
+    heads = [(0, hh) for hh in range(w.H)]
+    rdk = U.map_heads(lambda bb, hh: U.oracle_last_keys_dk(inp, w, bb, hh, 2, R), heads, threads=4)
     q1, k1, q2, k2 = U.dev_inputs(inp)
     for mode in (skl.BWD_AUTO, skl.BWD_SEPARATE):
         dq, dk = _run_bwd(inp, w, 2, mode, kl, l1, l2)
         torch.cuda.synchronize()
         U.assert_grad(U.np64(dq)[b, h, i], rdq, f"mode {mode}: dQ1 sampled rows")
-        r_sum, r_tr = U.dk_invariants(dk, k1, dq, q1)
-        assert r_sum < 2e-2 and r_tr < 2e-2, (mode, r_sum, r_tr)
+        for (bb, hh), ref in zip(heads, rdk):
+            U.assert_grad(U.np64(dk[bb, hh, -R:]), ref, f"mode {mode}: dK1 last {R} keys head {bb},{hh}")
+        U.assert_dk_invariants(dk, k1, dq, q1, 2, f"mode {mode}")
         del dq, dk
 
 

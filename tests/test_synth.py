@@ -42,3 +42,10 @@ def test_pair_counts_and_samples():
     assert len({tuple(r) for r in rows}) == 256
     for i in (0, 1, 127, 128, 65535):
         assert i in set(rows[:, 2].tolist())
+
+
+def test_head_rows_is_a_prefix_of_the_head():
+    w = synth.WORKLOADS["kl_b1h1_n128_d64"].with_(B=2, H=2, NQ=50, NK=70)
+    for k in ("q1", "k1", "q2", "k2"):
+        full = synth.head_slice(w, k, 1, 1)
+        assert np.array_equal(synth.head_rows(w, k, 1, 1, 17), full[:17])
