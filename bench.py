@@ -61,6 +61,9 @@ def parse():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--heads", type=int, default=0, help="override H (smaller cases for profiling)")
     ap.add_argument("--batch", type=int, default=0, help="override B (smaller cases for profiling)")
+    ap.add_argument("--no-decode", action="store_true",
+                    help="training workloads: skip the Split-K decode section of the JSON line")
+    ap.add_argument("--decode-steps", type=int, default=10)
     ap.add_argument("--layout", default="bhnd", choices=["bhnd", "bnhd"],
                     help="storage of Q/K: contiguous [B,H,N,D], or [B,N,H,D] read in place through strides")
     return ap.parse_args()
@@ -250,6 +253,65 @@ def run_reference(args):
             "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
     return 0
+
+
+# ----------------------------------------------------------------------------- decode section
+
+DECODE_NQ = (1, 4, 16)
+
+
+def time_decode(args, dev, peaks, peak_src):
+    """Split-K and non-split forward on the decode workloads (B8 H32 N_K=131072 D128, N_Q = 1, 4, 16).
+
+    The three workloads share their keys (the same seed and per-head streams),
+    and the N_Q = 1 and 4 queries are the first rows of the N_Q = 16 ones, so
+    one set of inputs is generated.  K1 + K2 (17.2 GB) is far larger than L2.
+    Each variant: W warm-up calls, then `decode_steps` calls timed with CUDA
+    events on the launching stream; the clock sampler runs over the section.
+    """
+    import torch
+    import attention_kl_divergence_streamkl_gb300 as skl
+    from attention_kl_divergence_streamkl_gb300 import synth
+
+    w16 = synth.WORKLOADS["decode_b8h32_nq16_nk131072_d128"]
+    inp = synth.make_inputs(w16)
+    dev_t = {k: torch.from_numpy(inp[k].view(np.int16)).view(torch.bfloat16).to(dev) for k in ("q1", "k1", "q2", "k2")}
+    del inp
+    stream = torch.cuda.current_stream(dev)
+    scale = w16.softmax_scale
+    out = {}
+    sampler = ClockSampler(gpu_id_for(dev.index))
+    torch.cuda.synchronize(dev)
+    sampler.start()
+    for nq in DECODE_NQ:
+        q1 = dev_t["q1"][:, :, :nq].contiguous()
+        q2 = dev_t["q2"][:, :, :nq].contiguous()
+        k1, k2 = dev_t["k1"], dev_t["k2"]
+        nbytes = 2 * w16.B * w16.H * w16.NK * w16.D * 2 + 2 * w16.B * w16.H * nq * w16.D * 2
+        row = {"workload": f"decode_b8h32_nq{nq}_nk131072_d128", "bytes_per_call": nbytes}
+        for name, fn in (("splitk", lambda: skl.fwd_splitk(q1, k1, q2, k2, scale, False)),
+                         ("nonsplit", lambda: skl.fwd(q1, k1, q2, k2, scale, False))):
+            for _ in range(args.warmup):
+                fn()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize(dev)
+            e0.record(stream)
+            for _ in range(args.decode_steps):
+                fn()
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            ms = e0.elapsed_time(e1) / args.decode_steps
+            gbs = nbytes / (ms / 1e3) / 1e9
+            row[name] = {"ms": ms, "GB/s": gbs, "frac_hbm": gbs / peaks["hbm_gbs"]}
+        out[str(nq)] = row
+    clocks = sampler.stop()
+    assert skl.check_device_status(dev) == 0, "device-side timeout in the decode section"
+    del dev_t
+    torch.cuda.empty_cache()
+    return {"metric": "attn-KL split-K decode fwd GB/s (B8 H32 N_K=131072 D128)", "unit": "GB/s",
+            "peak": peaks["hbm_gbs"], "peak_source": f"{peak_src} hbm_gbs", "steps": args.decode_steps,
+            "warmup": args.warmup, "launches_per_call": {"splitk": 2, "nonsplit": 1}, "nq": out, "clocks": clocks,
+            "l2": "inputs larger than L2, no flush between calls"}
 
 
 # ----------------------------------------------------------------------------- our arm
@@ -457,6 +519,13 @@ def run_ours(args):
             cpu = {"value": v, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle", "sample": desc,
                    "seconds": dt}
 
+    decode_section = None
+    if not decode and not args.no_decode and args.workload == "kl_b1h32_n65536_d128_causal" and not (
+            args.heads or args.batch):
+        del q1, k1, q2, k2
+        torch.cuda.empty_cache()
+        decode_section = time_decode(args, dev, peaks, peak_src)
+
     line = {"metric": metric, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
@@ -470,6 +539,8 @@ def run_ours(args):
                        "parallelism": f"replicas{world}"},
             "roofline": roof, "per_kernel_ms": {k: v / args.steps for k, v in per_kernel.items()},
             "gpu_launches": launches_per_step * args.steps, "clocks": clocks, "e2e": e2e, "cpu_baseline": cpu}
+    if decode_section is not None:
+        line["decode"] = decode_section
     if rank == 0:
         print(json.dumps(line))
     if world > 1:

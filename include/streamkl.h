@@ -27,6 +27,8 @@
  *   rejected so that no row is left without keys.
  * - The caller owns every buffer; the library allocates no device memory.
  *   Scratch memory is passed in as a workspace whose size is queried first.
+ *   The one exception is streamkl_fwd_splitk_noalloc, whose scratch is a
+ *   fixed static device array inside the library.
  * - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls are
  *   asynchronous on it.  Argument errors are returned synchronously before
  *   anything is launched.  Launch failures return STREAMKL_ERR_CUDA.
@@ -130,9 +132,13 @@ streamkl_status streamkl_fwd_splitk_plan(streamkl_shape s, int num_sms, int* num
  * the library keeps it until the process exits.  A problem whose partials
  * (B*H*N_Q*splits*5 floats) do not fit returns STREAMKL_ERR_SCRATCH_LIMIT with
  * nothing launched.  All calls share that array and it keeps the last call's
- * contents (each call overwrites every value it reads, so nothing needs
- * clearing); calls that overlap on the GPU -- on different streams, or from
- * different host threads -- race on it and must be serialised by the caller.
+ * contents: a call that completes writes every partial it then reads, so
+ * nothing needs clearing.  If one of its bounded waits runs out, a partial
+ * block stops without writing and the merge reads what an earlier call left
+ * there, so the outputs are valid only when streamkl_check_device_status
+ * returns STREAMKL_OK afterwards.  Calls that overlap on the GPU -- on
+ * different streams, or from different host threads -- race on the array
+ * and must be serialised by the caller.
  * The first call on a device looks up the array's device address with that
  * device current (once per device); make that first call before any stream
  * capture.  Results equal streamkl_fwd_splitk's for the same num_splits.
@@ -201,6 +207,12 @@ const char* streamkl_status_string(streamkl_status st);
  * Synchronises `stream`, then reads and clears the device status word of the
  * current device.  Returns STREAMKL_ERR_TIMEOUT if a bounded wait ran out since
  * the last check, STREAMKL_ERR_CUDA if the sync failed, else STREAMKL_OK.
+ *
+ * The status word is one flag per device for the whole process, shared by
+ * every caller, stream and thread that uses the library: a timeout on any
+ * stream sets it, and the first check afterwards -- from whichever thread --
+ * reports and clears it.  Callers that share a device and each want to see
+ * their own timeouts must serialise their checks (or agree on one checker).
  */
 streamkl_status streamkl_check_device_status(void* stream);
 

@@ -36,13 +36,17 @@ def _noalloc(L, ins, w, splits):
 
 
 def test_noalloc_splitk_matches_workspace_entry_point_on_two_calls():
+    """Two calls in a row on different problems: the second (fewer heads, other split count, other values)
+    finds the first one's partials in the shared scratch and must still match the workspace entry point on
+    its own inputs, so a partial that the second call failed to write would show up."""
     build.build()
     L = skl.lib()
-    w = synth.Workload("noalloc", 2, 8, 5, 3000, 128, True, 0.5, 21)
-    ins = U.dev_inputs(synth.make_inputs(w))
-    ref = skl.fwd_splitk(*ins, w.softmax_scale, w.causal, num_splits=7)
-    for call in range(2):  # the second call finds the first call's partials in the scratch
-        st, out = _noalloc(L, ins, w, 7)
+    problems = [(synth.Workload("noalloc", 2, 8, 5, 3000, 128, True, 0.5, 21), 7),
+                (synth.Workload("noalloc_b", 1, 6, 4, 2900, 128, False, 0.5, 23), 5)]
+    for call, (w, splits) in enumerate(problems):
+        ins = U.dev_inputs(synth.make_inputs(w))
+        ref = skl.fwd_splitk(*ins, w.softmax_scale, w.causal, num_splits=splits)
+        st, out = _noalloc(L, ins, w, splits)
         assert st == K.OK, K.status_string(st)
         torch.cuda.synchronize()
         U.assert_rows(*(U.np64(x) for x in out), *(U.np64(x) for x in ref), f"call {call}")
