@@ -11,14 +11,20 @@
 //
 // Block = one 128-query tile (stationary Q1, Q2 in smem; queries on the 128 TMEM
 // lanes), streaming 128-key tiles.  Every MMA is M = 128, N = 128 (a single-CTA
-// M = 128 MMA costs the same for any N up to 128 on this GPU):
+// M128 K16 MMA runs 48 cycles at N = 64 and 64 at N = 128, the full tensor rate):
 //   S_a = Q_a K_a^T, then S_b = Q_b K_b^T  SS, K-major, both into TMEM columns [0, 128);
 //                                          b = opt (2 in setting 1, 1 in setting 2), a = the other
 //   dS from S and the row's folded LSE1, LSE2, g, KL; to smem as dS[query][key]
 //   dQ   += dS K_opt                    SS: A = dS (K-major over keys), B = K_opt MN-major  -> [128, 128 + D)
 //   dKp^T = Q_opt^T dS                  SS: A = Q_opt read MN-major (M = d), B = dS MN-major -> [256 + 128 b, ...)
 //   dk_acc[key, d] += dKp^T[d, key]     one warp adds 32 consecutive d of one key row (128 B) per red
-// The MMAs of key tile j are issued as S_a(j), dQ(j - 1), S_b(j), dKp(j - 1).
+// Two threads issue the MMAs, each from its own warp: one the logits S_a(j),
+// S_b(j) of every key tile, the other the gradient MMAs dQ(j), dKp(j) once dS(j)
+// is in shared memory.  A tcgen05.mma takes a single issuing thread several
+// tens of cycles to issue, close to the 64 cycles an M128 N128 K16 MMA runs,
+// so one thread that also waits on every hand-off leaves the tensor pipe idle;
+// two threads on different SMSPs keep it fed, and a gradient MMA waiting for
+// its dK buffer no longer holds up the next tile's logits.
 // The dS warps copy S_a into registers (in setting 1 they turn it into P1 while
 // S_b is in flight), S_b is written over it and read in two halves.  A thread
 // owns a query row, so its per-query values sit in registers
@@ -28,10 +34,13 @@
 //   warps 0-15  dS warps: thread = query row (lane quarter = warp % 4), group g = warp / 4
 //               takes key columns [32g, 32g + 32); at the end they write dQ
 //   warp 16     TMA producer: Q1, Q2 once, the other K tile through two slots
-//   warp 17     TMEM owner and MMA issuer
+//   warp 17     TMEM owner and issuer of the logits MMAs
 //   warp 18     TMA producer of K_opt (two slots, each held until the gradient MMAs)
-//   warps 20-23 dK warps: thread = column d of dKp^T, reduce-add into dk_acc
-// Warpgroups 4-5 give registers to the dS warpgroups (setmaxnreg).
+//   warp 19     issuer of the gradient MMAs
+//   warps 20-27 dK warps: thread = column d of dKp^T (lane quarter = warp % 4), warps
+//               20-23 take keys [0, 64) of a tile and 24-27 keys [64, 128); they
+//               reduce-add into dk_acc (two per SMSP keep more reductions in flight)
+// Warpgroups 4-6 give registers to the dS warpgroups (setmaxnreg).
 #include <algorithm>
 #include <utility>
 
@@ -50,9 +59,11 @@ constexpr int DS_WARPS = 16;
 constexpr int PRODUCER_WARP = 16;
 constexpr int MMA_WARP = 17;
 constexpr int KOPT_WARP = 18;
+constexpr int GRAD_WARP = 19;
 constexpr int DK_WARP0 = 20;
-constexpr int THREADS = 24 * 32;
-constexpr int kRegsDs = 88, kRegsOther = 64;  // 512 * 88 + 256 * 64 = 768 * 80 registers at launch
+constexpr int DK_WARPS = 8;
+constexpr int THREADS = 28 * 32;
+constexpr int kRegsDs = 80, kRegsOther = 56;  // 512 * 80 + 384 * 56 <= 896 * 72 registers at launch
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0, kColDQ = 128, kColDK = 256;  // dKp^T buffer b at kColDK + 128 b
 
@@ -67,9 +78,9 @@ struct Smem {
   static constexpr int OFF_DS = OFF_KT + SLOTS * TK;  // dS[query][key] bf16: 2 halves of [128 queries][128 B]
   static constexpr int DS_BYTES = BQ * BK * 2;
   static constexpr int OFF_BAR = OFF_DS + DS_BYTES;
-  // mbarriers (8 B each): q_full, ko_full[2], ko_empty[2], kt_full[2], kt_empty[2], sa_full, sa_free,
-  // sb_full, sb_free, ds_full, ds_free, dk_full[2], dk_free[2], all_done; then the TMEM base address
-  // slot and the abort flag
+  // mbarriers (8 B each): q_full, ko_full[2], ko_empty[2] (S_b and dQ both arrive), kt_full[2],
+  // kt_empty[2], sa_full, sa_free, sb_full, sb_free, ds_full, ds_free, dk_full[2], dk_free[2],
+  // all_done; then the TMEM base address slot and the abort flag
   static constexpr int BAR_SLOT = 20 * 8;
   static constexpr int BYTES = OFF_BAR + BAR_SLOT + 16 + 1024;
 };
@@ -141,7 +152,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     mbar_init(q_full, 1);
     for (int s = 0; s < SLOTS; ++s) {
       mbar_init(ko_full + 8 * s, 1);
-      mbar_init(ko_empty + 8 * s, 1);
+      mbar_init(ko_empty + 8 * s, 2);
       mbar_init(kt_full + 8 * s, 1);
       mbar_init(kt_empty + 8 * s, 1);
     }
@@ -153,7 +164,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     mbar_init(ds_free, 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(dk_full + 8 * b, 1);
-      mbar_init(dk_free + 8 * b, 4);
+      mbar_init(dk_free + 8 * b, DK_WARPS);
     }
     mbar_init(all_done, 1);
     *abort_flag = 0;
@@ -221,80 +232,83 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       __syncwarp();
     } else if (warp == MMA_WARP) {
-      // ------------------------------------------------------------------ MMA issuer
-      // Per key tile j: S_a(j); dQ of tile j - 1 (its dS is done before the dS warps
-      // read S_a(j), so it fills the tensor pipe while they do); S_b(j) once they
-      // hold S_a(j); then dKp of tile j - 1.  S_a(j + 1) then queues behind one
-      // gradient group, not two, and K_opt(j - 1) is released before S_b(j).
+      // ------------------------------------------------------------------ MMA issuer: logits
+      // S_a(j) once the dS warps have read S_b(j - 1) out of the shared region,
+      // S_b(j) once they hold S_a(j).
       if (lane == 0) {
         constexpr uint32_t id_s = idesc_bf16(BQ, BK, false, false);
+        const uint64_t qad = sdesc_sw128(sb + OFF_QA, 0, 1024), qbd = sdesc_sw128(sb + OFF_QB, 0, 1024);
+        bool ok = mbar_wait(q_full, 0, status, abort_flag);
+        for (int j = 0; ok && j < n_kt; ++j) {
+          const int s = j % SLOTS;
+          if (!mbar_wait(kt_full + 8 * s, (j / SLOTS) & 1, status, abort_flag)) break;
+          if (j >= 1 && !mbar_wait(sb_free, (j - 1) & 1, status, abort_flag)) break;
+          tc_fence_after();
+          const uint64_t kad = sdesc_sw128(sb + L::OFF_KT + s * L::TK, 0, 1024);
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks) {
+            const uint32_t off = (ks >> 2) * (128 * 128) + (ks & 3) * 32;  // BQ == BK: same half stride
+            mma_ss(tmem + kColS, sdesc_add(qad, off), sdesc_add(kad, off), id_s, ks > 0);
+          }
+          mma_commit(sa_full);
+          mma_commit(kt_empty + 8 * s);  // the other K tile is read only by S_a
+          if (!mbar_wait(sa_free, j & 1, status, abort_flag)) break;
+          if (!mbar_wait(ko_full + 8 * s, (j / SLOTS) & 1, status, abort_flag)) break;
+          tc_fence_after();
+          const uint64_t kbd = sdesc_sw128(sb + L::OFF_KO + s * L::TK, 0, 1024);
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks) {
+            const uint32_t off = (ks >> 2) * (128 * 128) + (ks & 3) * 32;
+            mma_ss(tmem + kColS, sdesc_add(qbd, off), sdesc_add(kbd, off), id_s, ks > 0);
+          }
+          mma_commit(sb_full);
+          mma_commit(ko_empty + 8 * s);  // first of the two arrivals that free K_opt(j)
+        }
+      }
+      __syncwarp();
+    } else if (warp == GRAD_WARP) {
+      // ------------------------------------------------------------------ MMA issuer: gradients
+      // dQ(j) and dKp(j) once dS(j) is in shared memory; dKp(j) also waits for
+      // its TMEM buffer (tile j - 2's) to be drained by the dK warps.
+      if (lane == 0) {
         constexpr uint32_t id_dq = idesc_bf16(BQ, D, false, true);
         constexpr uint32_t id_dk = idesc_bf16(128, BK, true, true);
-        const uint64_t qad = sdesc_sw128(sb + OFF_QA, 0, 1024), qbd = sdesc_sw128(sb + OFF_QB, 0, 1024);
         const uint64_t qod = sdesc_sw128(sb + OFF_QB, D == 128 ? BQ * 128 : 0, 1024);  // Q_opt as MN-major A
         const uint64_t dsk = sdesc_sw128(sb + L::OFF_DS, 0, 1024);         // dS as A of dQ (K-major over keys)
         const uint64_t dsm = sdesc_sw128(sb + L::OFF_DS, BQ * 128, 1024);  // dS as B of dKp (MN-major over keys)
         bool ok = mbar_wait(q_full, 0, status, abort_flag);
-        for (int j = 0; ok && j <= n_kt; ++j) {
-          const int s = j % SLOTS;
-          if (j < n_kt) {
-            if (!mbar_wait(kt_full + 8 * s, (j / SLOTS) & 1, status, abort_flag)) break;
-            if (j >= 1 && !mbar_wait(sb_free, (j - 1) & 1, status, abort_flag)) break;
-            tc_fence_after();
-            const uint64_t kad = sdesc_sw128(sb + L::OFF_KT + s * L::TK, 0, 1024);
+        for (int j = 0; ok && j < n_kt; ++j) {
+          const int s = j % SLOTS, b = j & 1;
+          if (!mbar_wait(ds_full, j & 1, status, abort_flag)) break;
+          // K_opt(j) has landed (S_b(j) read it before dS(j) existed); waited here too so that this
+          // thread's MMAs are ordered after the copy
+          if (!mbar_wait(ko_full + 8 * s, (j / SLOTS) & 1, status, abort_flag)) break;
+          tc_fence_after();
+          // dQ += dS K_opt: A = dS[query][key] K-major (key k-steps), B = K_opt read MN-major
+          const uint64_t kod = sdesc_sw128(sb + L::OFF_KO + s * L::TK, BK * 128, 1024);
 #pragma unroll
-            for (int ks = 0; ks < D / 16; ++ks) {
-              const uint32_t off = (ks >> 2) * (128 * 128) + (ks & 3) * 32;  // BQ == BK: same half stride
-              mma_ss(tmem + kColS, sdesc_add(qad, off), sdesc_add(kad, off), id_s, ks > 0);
-            }
-            mma_commit(sa_full);
-            mma_commit(kt_empty + 8 * s);  // the other K tile is read only by S_a
-          }
-          if (j >= 1) {
-            const int jj = j - 1, sp = jj % SLOTS;
-            if (!mbar_wait(ds_full, jj & 1, status, abort_flag)) break;
-            tc_fence_after();
-            // dQ += dS K_opt: A = dS[query][key] K-major (key k-steps), B = K_opt read MN-major
-            const uint64_t kod = sdesc_sw128(sb + L::OFF_KO + sp * L::TK, BK * 128, 1024);
+          for (int ks = 0; ks < BK / 16; ++ks)
+            mma_ss(tmem + kColDQ, sdesc_add(dsk, (ks >> 2) * (BQ * 128) + (ks & 3) * 32), sdesc_add(kod, ks * 2048),
+                   id_dq, j > 0 || ks > 0);
+          mma_commit(ko_empty + 8 * s);  // second arrival: K_opt(j) was read by S_b(j) and this dQ
+          // dKp^T buffer b was drained (tile j - 2) by the dK warps
+          if (j >= 2 && !mbar_wait(dk_free + 8 * b, ((j >> 1) - 1) & 1, status, abort_flag)) break;
+          tc_fence_after();
+          // dKp^T = Q_opt^T dS: A = Q_opt (queries x d) read MN-major, B = dS (queries x keys) MN-major
 #pragma unroll
-            for (int ks = 0; ks < BK / 16; ++ks)
-              mma_ss(tmem + kColDQ, sdesc_add(dsk, (ks >> 2) * (BQ * 128) + (ks & 3) * 32), sdesc_add(kod, ks * 2048),
-                     id_dq, jj > 0 || ks > 0);
-            mma_commit(ko_empty + 8 * sp);  // K_opt(jj) was read by S_b(jj) and this dQ
-          }
-          if (j < n_kt) {
-            if (!mbar_wait(sa_free, j & 1, status, abort_flag)) break;
-            if (!mbar_wait(ko_full + 8 * s, (j / SLOTS) & 1, status, abort_flag)) break;
-            tc_fence_after();
-            const uint64_t kbd = sdesc_sw128(sb + L::OFF_KO + s * L::TK, 0, 1024);
-#pragma unroll
-            for (int ks = 0; ks < D / 16; ++ks) {
-              const uint32_t off = (ks >> 2) * (128 * 128) + (ks & 3) * 32;
-              mma_ss(tmem + kColS, sdesc_add(qbd, off), sdesc_add(kbd, off), id_s, ks > 0);
-            }
-            mma_commit(sb_full);
-          }
-          if (j >= 1) {
-            const int jj = j - 1, b = jj & 1;
-            // dKp^T buffer b was drained (tile jj - 2) by the dK warps
-            if (jj >= 2 && !mbar_wait(dk_free + 8 * b, ((jj >> 1) - 1) & 1, status, abort_flag)) break;
-            tc_fence_after();
-            // dKp^T = Q_opt^T dS: A = Q_opt (queries x d) read MN-major, B = dS (queries x keys) MN-major
-#pragma unroll
-            for (int ks = 0; ks < BQ / 16; ++ks)
-              mma_ss(tmem + kColDK + 128 * b, sdesc_add(qod, ks * 2048), sdesc_add(dsm, ks * 2048), id_dk, ks > 0);
-            mma_commit(ds_free);
-            mma_commit(dk_full + 8 * b);
-          }
+          for (int ks = 0; ks < BQ / 16; ++ks)
+            mma_ss(tmem + kColDK + 128 * b, sdesc_add(qod, ks * 2048), sdesc_add(dsm, ks * 2048), id_dk, ks > 0);
+          mma_commit(ds_free);
+          mma_commit(dk_full + 8 * b);
         }
-        // every MMA done: arrives on all_done (waited by the dQ epilogue and below)
+        // every gradient MMA done: arrives on all_done (waited by the dQ epilogue and below)
         mma_commit(all_done);
         mbar_drain(all_done, 0, status);
       }
       __syncwarp();
     } else if (warp >= DK_WARP0) {
       // ------------------------------------------------------------------ dK warps
-      const int wq = warp - DK_WARP0;
+      const int wq = (warp - DK_WARP0) & 3, half = (warp - DK_WARP0) >> 2;
       const int d = wq * 32 + lane;  // lane of dKp^T = column d
       const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
       for (int j = 0; j < n_kt; ++j) {
@@ -306,13 +320,14 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int k0 = kbase + j * BK;
         float* base = dk_acc + ((size_t)bh * kr.dk_rows + j * BK) * D + d;
 #pragma unroll 1
-        for (int cb = 0; cb < BK / 32; ++cb) {
+        for (int cb = 2 * half; cb < 2 * half + 2; ++cb) {  // this warp's half of the keys
           uint32_t v[32];
           tmem_ld32(tmem + lane_base + kColDK + 128 * b + 32 * cb, v);
           tmem_ld_wait();
           reg_fence32(v);
-          if (cb == BK / 32 - 1) {
-            // the whole dKp^T tile has been read: the dKp MMA of tile j + 2 may overwrite it
+          if (cb == 2 * half + 1) {
+            // this warp's half of the dKp^T tile has been read: once all eight warps have, the
+            // dKp MMA of tile j + 2 may overwrite it
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(dk_free + 8 * b);

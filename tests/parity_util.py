@@ -172,16 +172,20 @@ def dk_invariants(dk, k_opt, dq, q_opt):
       settings.  Residual |sum_j dK_jd| / sum_j |dK_jd|; a column that is all
       zero scores inf, so a zero dK fails.
     * the trace identity sum_i <dQ_i, Q_i> = sum_j <dK_j, K_j> per (b, h)
-      (both sides equal sum_ij dS_ij S_ij).  The residual is taken against the
-      root-sum-square of the element products dQ*Q and dK*K: bf16 rounding of
-      the outputs moves each side by about 2^-9/sqrt(3) of that, whatever the
-      cancellation inside the sums.
+      (both sides equal sum_ij dS_ij S_ij, for any dS, so the kernels' own bf16
+      dS obeys it too).  Its residual is divided by the error the arithmetic
+      allows: TRACE_TOL x the root-sum-square of the element products dQ*Q and
+      dK*K (bf16 rounding of the outputs moves each side by about 2^-9/sqrt(3)
+      of that), plus delta x the sum of their magnitudes, delta = 2^-23 per
+      128-wide step of the longer fp32 accumulation (one ulp per step: the
+      accumulator's rounding need not be unbiased, so this part adds up
+      linearly).  A residual below 1 passes.
 
     Returns (r_sum, r_tr, power): the worst residuals over heads, and the
-    smallest |sum_i <dQ_i, Q_i>| / rss over heads -- what a dK of zero (or of
-    the wrong scale) would score on the trace identity.  In setting 1 the sum
-    has no cancellation (power ~ 200 at 4K keys), so the identity pins dK's
-    scale on every head; in setting 2 it cancels (power down to ~0.01) and the
+    smallest |sum_i <dQ_i, Q_i>| / allowed error over heads -- what a dK of
+    zero would score on the trace identity.  In setting 1 the sum has no
+    cancellation (power in the thousands), so the identity pins dK's scale on
+    every head; in setting 2 it cancels (power can drop below 1) and the
     identity only bounds dK's errors.
     """
     dk = dk.double()
@@ -193,18 +197,22 @@ def dk_invariants(dk, k_opt, dq, q_opt):
     tk = dk * k_opt.double()
     lhs, rhs = tq.sum(dim=(2, 3)), tk.sum(dim=(2, 3))
     rss = ((tq * tq).sum(dim=(2, 3)) + (tk * tk).sum(dim=(2, 3))).sqrt()
-    ok = rss > 0
-    r_tr = float(torch.where(ok, (lhs - rhs).abs() / rss.clamp_min(1e-300), torch.full_like(rss, math.inf)).max())
-    power = float(torch.where(ok, lhs.abs() / rss.clamp_min(1e-300), torch.zeros_like(rss)).min())
+    steps = max(-(-dq.shape[2] // 128), -(-dk.shape[2] // 128))
+    delta = steps * 2.0 ** -23
+    allowed = TRACE_TOL * rss + delta * (tq.abs().sum(dim=(2, 3)) + tk.abs().sum(dim=(2, 3)))
+    ok = allowed > 0
+    r_tr = float(torch.where(ok, (lhs - rhs).abs() / allowed.clamp_min(1e-300), torch.full_like(rss, math.inf)).max())
+    power = float(torch.where(ok, lhs.abs() / allowed.clamp_min(1e-300), torch.zeros_like(rss)).min())
     return r_sum, r_tr, power
 
 
 def assert_dk_invariants(dk, k_opt, dq, q_opt, setting, what=""):
     r_sum, r_tr, power = dk_invariants(dk, k_opt, dq, q_opt)
+    print(f"{what}: dK identities r_sum {r_sum:.3e} r_tr {r_tr:.3e} power {power:.3e}")
     assert r_sum < TRACE_TOL, f"{what}: sum_j dK_j residual {r_sum:.3e}"
-    assert r_tr < TRACE_TOL, f"{what}: trace identity residual {r_tr:.3e}"
+    assert r_tr < 1.0, f"{what}: trace identity residual {r_tr:.3e} of the allowed error"
     if setting == 1:
-        assert power > 10 * TRACE_TOL, f"{what}: trace identity cannot see dK's scale (power {power:.3e})"
+        assert power > 10.0, f"{what}: trace identity cannot see dK's scale (power {power:.3e})"
     return r_sum, r_tr, power
 
 
