@@ -47,6 +47,7 @@ class StreamKLError(RuntimeError):
 
 
 _P, _F, _S, _I, _SZ = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+_LL = ctypes.c_longlong
 # name -> (restype, argtypes); also the list of symbols include/streamkl.h declares
 SIGNATURES = {
     "streamkl_fwd": (_I, [_P, _P, _P, _P, Shape, _F, _F, _F, _S]),
@@ -54,6 +55,11 @@ SIGNATURES = {
     "streamkl_fwd_splitk": (_I, [_P, _P, _P, _P, Shape, _I, _P, _SZ, _F, _F, _F, _S]),
     "streamkl_fwd_splitk_plan": (_I, [Shape, _I, ctypes.POINTER(_I)]),
     "streamkl_fwd_splitk_noalloc": (_I, [_P, _P, _P, _P, Shape, _I, _F, _F, _F, _S]),
+    "streamkl_fwd_partials": (_I, [_P, _P, _P, _P, Shape, _LL, _LL, _F, _S]),
+    "streamkl_merge_partials": (_I, [_F, _I, Shape, _F, _F, _F, _S]),
+    "streamkl_bwd_keyshard_workspace": (_I, [Shape, _LL, _LL, ctypes.POINTER(_SZ)]),
+    "streamkl_bwd_keyshard": (_I, [_I, _P, _P, _P, _P, Shape, _LL, _LL, _F, _F, _F, _F, _F, _P, _P, _SZ, _S]),
+    "streamkl_dq_from_partial": (_I, [_F, Shape, _P, _S]),
     "streamkl_bwd_workspace": (_I, [Shape, _I, ctypes.POINTER(_SZ)]),
     "streamkl_bwd_select": (_I, [Shape, _SZ, _I]),
     "streamkl_bwd_fused_plan": (_I, [Shape, _SZ, _I, ctypes.POINTER(_I), ctypes.POINTER(_SZ)]),
@@ -224,6 +230,75 @@ def fwd_splitk(q1, k1, q2, k2, scale=None, causal=False, num_splits=0):
                                      nbytes.value, _ptr(kl), _ptr(l1), _ptr(l2), _stream(q1.device)),
            "streamkl_fwd_splitk")
     return _back((kl, l1, l2), host)
+
+
+def fwd_partials(q1, k1, q2, k2, key_offset, nk_total, scale=None, causal=False):
+    """Five scalars per row fp32 [B, H, N_Q, 5] over a key shard.
+
+    k1, k2 hold the shard's keys, at global positions [key_offset, key_offset +
+    k1.shape[2]) of a sequence of nk_total keys (the causal frontier is the
+    global one).  Merge the shards' partials with merge_partials."""
+    (q1, k1, q2, k2), host, qs, ks = _prep(q1, k1, q2, k2)
+    B, H, NQ, D = q1.shape
+    s = make_shape(B, H, NQ, k1.shape[2], D, scale, causal, qs, ks)
+    part = torch.empty((B, H, NQ, 5), dtype=torch.float32, device=q1.device)
+    _check(lib().streamkl_fwd_partials(_ptr(q1), _ptr(k1), _ptr(q2), _ptr(k2), s, int(key_offset), int(nk_total),
+                                       _ptr(part), _stream(q1.device)), "streamkl_fwd_partials")
+    return _back((part,), host)[0]
+
+
+def merge_partials(parts, D, scale=None):
+    """KL, LSE1, LSE2 fp32 [B, H, N_Q] from partial sets stacked as [S, B, H, N_Q, 5] (device)."""
+    if parts.dtype != torch.float32 or parts.dim() != 5 or parts.shape[-1] != 5:
+        raise ValueError("partials must be float32 [S, B, H, N_Q, 5]")
+    parts = parts.contiguous()
+    S, B, H, NQ, _ = parts.shape
+    s = make_shape(B, H, NQ, 1, D, scale, False)
+    kl, l1, l2 = (torch.empty((B, H, NQ), dtype=torch.float32, device=parts.device) for _ in range(3))
+    _check(lib().streamkl_merge_partials(_ptr(parts), int(S), s, _ptr(kl), _ptr(l1), _ptr(l2),
+                                         _stream(parts.device)), "streamkl_merge_partials")
+    return kl, l1, l2
+
+
+def bwd_keyshard(setting, q1, k1, q2, k2, key_offset, nk_total, lse1, lse2, kl, g, scale=None, causal=False):
+    """Backward over a key shard: (unscaled fp32 dQ contribution [B, H, N_Q, D], bf16 dK of the shard's keys).
+
+    lse1, lse2, kl are the merged values of the whole sequence; summing the
+    dQ contributions of every shard and passing the sum to dq_from_partial gives dQ."""
+    (q1, k1, q2, k2), host, qs, ks = _prep(q1, k1, q2, k2)
+    B, H, NQ, D = q1.shape
+    NK = k1.shape[2]
+    dev = q1.device
+    s = make_shape(B, H, NQ, NK, D, scale, causal, qs, ks)
+    lse1 = _rows(lse1, dev, (B, H, NQ), "lse1")
+    lse2 = _rows(lse2, dev, (B, H, NQ), "lse2")
+    g = _rows(g, dev, (B, H, NQ), "g")
+    kl = _rows(kl, dev, (B, H, NQ), "kl") if setting == 2 else None
+    nbytes = ctypes.c_size_t(0)
+    _check(lib().streamkl_bwd_keyshard_workspace(s, int(key_offset), int(nk_total), ctypes.byref(nbytes)),
+           "streamkl_bwd_keyshard_workspace")
+    ws = torch.empty(max(16, nbytes.value), dtype=torch.uint8, device=dev)
+    dq = torch.empty((B, H, NQ, D), dtype=torch.float32, device=dev)
+    dk = _grad_like(k1, ks, NK)
+    _check(lib().streamkl_bwd_keyshard(int(setting), _ptr(q1), _ptr(k1), _ptr(q2), _ptr(k2), s, int(key_offset),
+                                       int(nk_total), _ptr(lse1), _ptr(lse2), _ptr(kl), _ptr(g), _ptr(dq), _ptr(dk),
+                                       _ptr(ws), nbytes.value, _stream(dev)), "streamkl_bwd_keyshard")
+    return _back((dq, dk), host)
+
+
+def dq_from_partial(dq_partial, q_like, scale=None):
+    """bf16 dQ = scale * dq_partial, with the layout the library gives q_like's gradient."""
+    if dq_partial.dtype != torch.float32 or dq_partial.dim() != 4:
+        raise ValueError("dq_partial must be float32 [B, H, N_Q, D]")
+    dq_partial = dq_partial.contiguous()
+    B, H, NQ, D = dq_partial.shape
+    qs = _bhn_strides(q_like) or (H * NQ * D, NQ * D, D)
+    s = make_shape(B, H, NQ, 1, D, scale, False, qs)
+    out = _grad_like(q_like, qs, NQ) if _bhn_strides(q_like) else torch.empty(
+        (B, H, NQ, D), dtype=torch.bfloat16, device=dq_partial.device)
+    _check(lib().streamkl_dq_from_partial(_ptr(dq_partial), s, _ptr(out), _stream(dq_partial.device)),
+           "streamkl_dq_from_partial")
+    return out
 
 
 def bwd_select(B, H, NQ, NK, D, l2_bytes, num_sms, causal=False) -> int:

@@ -87,6 +87,24 @@ streamkl_status validate(const streamkl_shape& s, Problem* p) {
   return STREAMKL_OK;
 }
 
+// A key shard: s.NK keys at global positions [key_offset, key_offset + NK) of a
+// sequence of nk_total keys, every query row of the problem.  The causal
+// frontier is the global one (row i keeps global key j <= i + nk_total - N_Q),
+// which for the shard's local keys is j_local <= i + off with the offset below;
+// it may be negative (rows that see none of the shard's keys).
+streamkl_status validate_shard(streamkl_shape s, long long key_offset, long long nk_total, Problem* p) {
+  if (key_offset < 0 || nk_total <= 0 || nk_total > kMaxRows || s.NK <= 0 || key_offset + s.NK > nk_total)
+    return STREAMKL_ERR_INVALID;
+  if (s.causal && s.NQ > nk_total) return STREAMKL_ERR_INVALID;
+  const int causal = s.causal;
+  s.causal = 0;
+  const streamkl_status v = validate(s, p);
+  if (v != STREAMKL_OK) return v;
+  p->causal = causal ? 1 : 0;
+  p->off = (int)(nk_total - s.NQ - key_offset);
+  return STREAMKL_OK;
+}
+
 bool inputs_ok(const void* q1, const void* k1, const void* q2, const void* k2) {
   return q1 && k1 && q2 && k2 && aligned16(q1) && aligned16(k1) && aligned16(q2) && aligned16(k2);
 }
@@ -299,6 +317,84 @@ streamkl_status streamkl_fwd_splitk_noalloc(const void* q1, const void* k1, cons
   if ((v = status_ptr(&status)) != STREAMKL_OK) return v;
   return from_cuda(launch_splitk(p, q1, k1, q2, k2, num_splits, scratch, kl, lse1, lse2, status,
                                  static_cast<cudaStream_t>(stream)));
+}
+
+streamkl_status streamkl_fwd_partials(const void* q1, const void* k1, const void* q2, const void* k2,
+                                      streamkl_shape s, long long key_offset, long long nk_total, float* partials,
+                                      void* stream) {
+  Problem p;
+  streamkl_status v = validate_shard(s, key_offset, nk_total, &p);
+  if (v != STREAMKL_OK) return v;
+  if (p.NQ == 0) return STREAMKL_OK;
+  if (!inputs_ok(q1, k1, q2, k2) || !rows_ok(partials)) return STREAMKL_ERR_INVALID;
+  int* status = nullptr;
+  if ((v = status_ptr(&status)) != STREAMKL_OK) return v;
+  return from_cuda(launch_fwd_partials(p, q1, k1, q2, k2, partials, status, static_cast<cudaStream_t>(stream)));
+}
+
+streamkl_status streamkl_merge_partials(const float* partials, int num_parts, streamkl_shape s, float* kl,
+                                        float* lse1, float* lse2, void* stream) {
+  Problem p;
+  s.causal = 0;  // only B, H, N_Q, D and the scale matter here
+  if (s.NK <= 0) s.NK = 1;
+  streamkl_status v = validate(s, &p);
+  if (v != STREAMKL_OK) return v;
+  if (num_parts < 1) return STREAMKL_ERR_INVALID;
+  if (p.NQ == 0) return STREAMKL_OK;
+  if (!rows_ok(partials) || !rows_ok(kl) || !rows_ok(lse1) || !rows_ok(lse2)) return STREAMKL_ERR_INVALID;
+  return from_cuda(launch_merge_partials(p, num_parts, partials, kl, lse1, lse2, static_cast<cudaStream_t>(stream)));
+}
+
+streamkl_status streamkl_bwd_keyshard_workspace(streamkl_shape s, long long key_offset, long long nk_total,
+                                                size_t* bytes) {
+  Problem p;
+  streamkl_status v = validate_shard(s, key_offset, nk_total, &p);
+  if (v != STREAMKL_OK) return v;
+  if (!bytes) return STREAMKL_ERR_INVALID;
+  size_t l2 = 0;
+  int sms = 0;
+  if ((v = device_l2_bytes(&l2)) != STREAMKL_OK || (v = device_sms(&sms)) != STREAMKL_OK) return v;
+  const int tiles = fused_range_tiles(p, l2, sms);
+  *bytes = (size_t)p.BH * std::min<long long>((long long)tiles * 128, p.NK) * p.D * sizeof(float);
+  return STREAMKL_OK;
+}
+
+streamkl_status streamkl_bwd_keyshard(int setting, const void* q1, const void* k1, const void* q2, const void* k2,
+                                      streamkl_shape s, long long key_offset, long long nk_total, const float* lse1,
+                                      const float* lse2, const float* kl, const float* g, float* dq_partial,
+                                      void* dk, void* workspace, size_t workspace_bytes, void* stream) {
+  Problem p;
+  streamkl_status v = validate_shard(s, key_offset, nk_total, &p);
+  if (v != STREAMKL_OK) return v;
+  if (setting != 1 && setting != 2) return STREAMKL_ERR_INVALID;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (!dk || !aligned16(dk)) return STREAMKL_ERR_INVALID;
+  if (p.NQ == 0) return from_cuda(cudaMemsetAsync(dk, 0, (size_t)p.BH * p.NK * p.D * 2, st));
+  if (!inputs_ok(q1, k1, q2, k2) || !rows_ok(lse1) || !rows_ok(lse2) || !rows_ok(g)) return STREAMKL_ERR_INVALID;
+  if (setting == 2 && !rows_ok(kl)) return STREAMKL_ERR_INVALID;
+  if (!dq_partial || !aligned16(dq_partial)) return STREAMKL_ERR_INVALID;
+  if (!workspace || !aligned16(workspace)) return STREAMKL_ERR_WORKSPACE;
+  size_t l2 = 0;
+  int sms = 0;
+  if ((v = device_l2_bytes(&l2)) != STREAMKL_OK || (v = device_sms(&sms)) != STREAMKL_OK) return v;
+  const int range_tiles = fused_range_tiles(p, l2, sms);
+  const size_t need = (size_t)p.BH * std::min<long long>((long long)range_tiles * 128, p.NK) * p.D * sizeof(float);
+  if (workspace_bytes < need) return STREAMKL_ERR_WORKSPACE;
+  int* status = nullptr;
+  if ((v = status_ptr(&status)) != STREAMKL_OK) return v;
+  BwdIn in{q1, k1, q2, k2, lse1, lse2, kl, g};
+  return from_cuda(launch_bwd_fused(p, setting, in, nullptr, dk, static_cast<float*>(workspace), range_tiles, status,
+                                    st, dq_partial));
+}
+
+streamkl_status streamkl_dq_from_partial(const float* dq_partial, streamkl_shape s, void* dq, void* stream) {
+  Problem p;
+  s.causal = 0;
+  streamkl_status v = validate(s, &p);
+  if (v != STREAMKL_OK) return v;
+  if (p.NQ == 0) return STREAMKL_OK;
+  if (!dq_partial || !aligned16(dq_partial) || !dq || !aligned16(dq)) return STREAMKL_ERR_INVALID;
+  return from_cuda(launch_rows_to_bf16(p, dq_partial, dq, static_cast<cudaStream_t>(stream)));
 }
 
 int streamkl_bwd_select(streamkl_shape s, size_t l2_bytes, int num_sms) {

@@ -542,35 +542,45 @@ int first_qtile(const Problem& p, long long k0) {
 
 template <int D>
 cudaError_t fused_d(const Problem& p, int setting, const BwdIn& in, void* dq, void* dk, float* ws, int range_tiles,
-                    int* status, cudaStream_t st) {
+                    int* status, cudaStream_t st, float* dq_f32) {
   const int n_kt = (p.NK + BK - 1) / BK;
   const int n_ranges = (n_kt + range_tiles - 1) / range_tiles;
   const int dk_rows = std::min(range_tiles * BK, p.NK);
   float* dk_acc = ws;
-  float* dq_acc = n_ranges > 1 ? ws + (size_t)p.BH * dk_rows * D : nullptr;
+  float* dq_acc = dq_f32 ? dq_f32 : (n_ranges > 1 ? ws + (size_t)p.BH * dk_rows * D : nullptr);
+  if (dq_f32) {
+    // every range adds into the caller's buffer: query tiles that see no key of these keys stay zero
+    cudaError_t e = cudaMemsetAsync(dq_f32, 0, (size_t)p.BH * p.NQ * D * sizeof(float), st);
+    if (e != cudaSuccess) return e;
+  }
   for (int r = 0; r < n_ranges; ++r) {
     const int jt0 = r * range_tiles, jt1 = std::min(n_kt, jt0 + range_tiles);
     const int k0 = jt0 * BK, nk = std::min(p.NK, jt1 * BK) - k0;
     cudaError_t e = cudaMemsetAsync(dk_acc, 0, (size_t)p.BH * dk_rows * D * sizeof(float), st);
     if (e != cudaSuccess) return e;
-    const KeyRange kr{jt0, jt1, first_qtile(p, k0), n_ranges == 1 ? DQ_BF16 : (r == 0 ? DQ_STORE : DQ_ADD), dk_rows,
-                      dq_acc};
+    const int dq_mode = dq_f32 ? DQ_ADD : (n_ranges == 1 ? DQ_BF16 : (r == 0 ? DQ_STORE : DQ_ADD));
+    const KeyRange kr{jt0, jt1, first_qtile(p, k0), dq_mode, dk_rows, dq_acc};
     e = setting == 1 ? launch_fused<D, 1>(p, kr, in, dq, dk_acc, status, st)
                      : launch_fused<D, 2>(p, kr, in, dq, dk_acc, status, st);
     if (e != cudaSuccess) return e;
     e = convert_rows<D>(dk_acc, dk, p, dk_rows, k0, nk, p.ks_b, p.ks_h, p.ks_n, st);
     if (e != cudaSuccess) return e;
   }
-  if (n_ranges > 1) return convert_rows<D>(dq_acc, dq, p, p.NQ, 0, p.NQ, p.qs_b, p.qs_h, p.qs_n, st);
+  if (!dq_f32 && n_ranges > 1) return convert_rows<D>(dq_acc, dq, p, p.NQ, 0, p.NQ, p.qs_b, p.qs_h, p.qs_n, st);
   return cudaSuccess;
 }
 
 }  // namespace
 
 cudaError_t launch_bwd_fused(const Problem& p, int setting, const BwdIn& in, void* dq, void* dk, float* workspace,
-                             int range_tiles, int* status, cudaStream_t st) {
-  if (p.D == 64) return fused_d<64>(p, setting, in, dq, dk, workspace, range_tiles, status, st);
-  return fused_d<128>(p, setting, in, dq, dk, workspace, range_tiles, status, st);
+                             int range_tiles, int* status, cudaStream_t st, float* dq_f32) {
+  if (p.D == 64) return fused_d<64>(p, setting, in, dq, dk, workspace, range_tiles, status, st, dq_f32);
+  return fused_d<128>(p, setting, in, dq, dk, workspace, range_tiles, status, st, dq_f32);
+}
+
+cudaError_t launch_rows_to_bf16(const Problem& p, const float* acc, void* out, cudaStream_t st) {
+  if (p.D == 64) return convert_rows<64>(acc, out, p, p.NQ, 0, p.NQ, p.qs_b, p.qs_h, p.qs_n, st);
+  return convert_rows<128>(acc, out, p, p.NQ, 0, p.NQ, p.qs_b, p.qs_h, p.qs_n, st);
 }
 
 int fused_first_qtile(const Problem& p, long long k0) { return first_qtile(p, k0); }

@@ -19,7 +19,9 @@
 // own maximum: if every term stays below 2^64 (the tile's sums show it, inf
 // included) the sums are kept, else the tile is redone with its maximum as
 // above.  At the end LSE_t = ln2 (m_t + log2 l_t) and KL = scale acc / l1 +
-// LSE2 - LSE1.
+// LSE2 - LSE1 -- or, for a key shard of a longer sequence, the five scalars
+// themselves are written out, to be merged with the other shards' (the
+// exact merge of the Split-K variant, section 手法 3).
 //
 // Block layout (one 128-row query tile per block, key tiles of 128):
 //   warp 8      TMA producer: Q1, Q2 once, then K1/K2 tiles through 2 stages
@@ -150,7 +152,8 @@ __device__ __forceinline__ void online_update(Row5& st, uint32_t (&a0)[32], uint
 template <int D>
 __global__ void __launch_bounds__(THREADS, 1)
     fwd_tc_kernel(const Problem p, float* __restrict__ out_kl, float* __restrict__ out_lse1,
-                  float* __restrict__ out_lse2, int* status, const __grid_constant__ CUtensorMap mq1,
+                  float* __restrict__ out_lse2, float* __restrict__ out_part, int* status,
+                  const __grid_constant__ CUtensorMap mq1,
                   const __grid_constant__ CUtensorMap mk1, const __grid_constant__ CUtensorMap mq2,
                   const __grid_constant__ CUtensorMap mk2) {
   using L = Smem<D>;
@@ -311,16 +314,26 @@ __global__ void __launch_bounds__(THREADS, 1)
       const float om1 = mrg[r], om2 = mrg[BM + r], ol1 = mrg[2 * BM + r], ol2 = mrg[3 * BM + r],
                   oacc = mrg[4 * BM + r];
       const float M1 = fmaxf(st.m1, om1), M2 = fmaxf(st.m2, om2);
-      const float wa1 = ex2(st.m1 - M1), wb1 = ex2(om1 - M1);
-      const float wa2 = ex2(st.m2 - M2), wb2 = ex2(om2 - M2);
+      // both groups empty only for a row that sees no key of a shard
+      const float wa1 = M1 == kNegInf ? 0.f : ex2(st.m1 - M1), wb1 = M1 == kNegInf ? 0.f : ex2(om1 - M1);
+      const float wa2 = M2 == kNegInf ? 0.f : ex2(st.m2 - M2), wb2 = M2 == kNegInf ? 0.f : ex2(om2 - M2);
       const float l1 = st.l1 * wa1 + ol1 * wb1, acc = st.acc * wa1 + oacc * wb1;
       const float l2 = st.l2 * wa2 + ol2 * wb2;
-      const float lse1 = (M1 + log2f(l1)) * kLn2;
-      const float lse2 = (M2 + log2f(l2)) * kLn2;
       const size_t o = (size_t)bh * p.NQ + row;
-      out_lse1[o] = lse1;
-      out_lse2[o] = lse2;
-      out_kl[o] = p.scale * (acc / l1) + lse2 - lse1;
+      if (out_part) {  // the row's five scalars over this shard's keys: m in log2 units, acc unscaled
+        float* d = out_part + o * 5;
+        d[0] = M1;
+        d[1] = M2;
+        d[2] = l1;
+        d[3] = l2;
+        d[4] = acc;
+      } else {
+        const float lse1 = (M1 + log2f(l1)) * kLn2;
+        const float lse2 = (M2 + log2f(l2)) * kLn2;
+        out_lse1[o] = lse1;
+        out_lse2[o] = lse2;
+        out_kl[o] = p.scale * (acc / l1) + lse2 - lse1;
+      }
     }
   }
   tc_fence_before();
@@ -333,7 +346,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 
 template <int D>
 cudaError_t launch_d(const Problem& p, const void* q1, const void* k1, const void* q2, const void* k2, float* kl,
-                     float* lse1, float* lse2, int* status, cudaStream_t st) {
+                     float* lse1, float* lse2, float* part, int* status, cudaStream_t st) {
   CUtensorMap mq1, mk1, mq2, mk2;
   if (!encode_q_map(&mq1, q1, p, BM) || !encode_q_map(&mq2, q2, p, BM) ||
       !encode_k_map(&mk1, k1, p, BN) || !encode_k_map(&mk2, k2, p, BN))
@@ -344,7 +357,7 @@ cudaError_t launch_d(const Problem& p, const void* q1, const void* k1, const voi
   cudaError_t e = cudaFuncSetAttribute(fwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const long long blocks = (long long)p.BH * ((p.NQ + BM - 1) / BM);
-  fwd_tc_kernel<D><<<(unsigned)blocks, THREADS, smem, st>>>(p, kl, lse1, lse2, status, mq1, mk1, mq2, mk2);
+  fwd_tc_kernel<D><<<(unsigned)blocks, THREADS, smem, st>>>(p, kl, lse1, lse2, part, status, mq1, mk1, mq2, mk2);
   return cudaGetLastError();
 }
 
@@ -352,8 +365,14 @@ cudaError_t launch_d(const Problem& p, const void* q1, const void* k1, const voi
 
 cudaError_t launch_fwd(const Problem& p, const void* q1, const void* k1, const void* q2, const void* k2,
                        float* kl, float* lse1, float* lse2, int* status, cudaStream_t st) {
-  if (p.D == 64) return launch_d<64>(p, q1, k1, q2, k2, kl, lse1, lse2, status, st);
-  return launch_d<128>(p, q1, k1, q2, k2, kl, lse1, lse2, status, st);
+  if (p.D == 64) return launch_d<64>(p, q1, k1, q2, k2, kl, lse1, lse2, nullptr, status, st);
+  return launch_d<128>(p, q1, k1, q2, k2, kl, lse1, lse2, nullptr, status, st);
+}
+
+cudaError_t launch_fwd_partials(const Problem& p, const void* q1, const void* k1, const void* q2, const void* k2,
+                                float* partials, int* status, cudaStream_t st) {
+  if (p.D == 64) return launch_d<64>(p, q1, k1, q2, k2, nullptr, nullptr, nullptr, partials, status, st);
+  return launch_d<128>(p, q1, k1, q2, k2, nullptr, nullptr, nullptr, partials, status, st);
 }
 
 }  // namespace skl

@@ -40,6 +40,14 @@ inline bool encode_k_map(CUtensorMap* map, const void* base, const Problem& p, i
 // ---- forward (one CTA per 128-row query tile) -------------------------------
 cudaError_t launch_fwd(const Problem& p, const void* q1, const void* k1, const void* q2, const void* k2,
                        float* kl, float* lse1, float* lse2, int* status, cudaStream_t st);
+// The same forward over one key shard (p.off already shifted by the shard's
+// first key): the five scalars of every row, fp32 [B*H*N_Q][5] (m1, m2 in log2
+// units, l1, l2, acc unscaled), instead of KL and LSE.
+cudaError_t launch_fwd_partials(const Problem& p, const void* q1, const void* k1, const void* q2, const void* k2,
+                                float* partials, int* status, cudaStream_t st);
+// Merges `parts` partial sets laid out [part][B*H*N_Q][5] into KL, LSE1, LSE2.
+cudaError_t launch_merge_partials(const Problem& p, int parts, const float* partials, float* kl, float* lse1,
+                                  float* lse2, cudaStream_t st);
 
 // ---- Split-K forward ---------------------------------------------------------
 constexpr int kSplitKTile = 64;        // keys per pipeline stage
@@ -64,8 +72,13 @@ cudaError_t launch_bwd_separate(const Problem& p, int setting, const BwdIn& in, 
 // range_tiles >= the tile count).  workspace: the fp32 dK rows of one range
 // ([B*H][min(128 range_tiles, N_K)][D]), then, with more than one range, the
 // fp32 dQ accumulator ([B*H][N_Q][D]).
+// With dq_f32 non-null, dQ is not written to dq: the unscaled fp32 sum over
+// this launch's keys goes to dq_f32 ([B*H][N_Q][D], zeroed first), and the
+// workspace holds only the dK rows of one range.
 cudaError_t launch_bwd_fused(const Problem& p, int setting, const BwdIn& in, void* dq, void* dk, float* workspace,
-                             int range_tiles, int* status, cudaStream_t st);
+                             int range_tiles, int* status, cudaStream_t st, float* dq_f32 = nullptr);
+// out row n of head bh = bf16(scale * acc[bh][n]) for n < N_Q, with Q's strides.
+cudaError_t launch_rows_to_bf16(const Problem& p, const float* acc, void* out, cudaStream_t st);
 // First 128-query tile whose rows see key k0.
 int fused_first_qtile(const Problem& p, long long k0);
 

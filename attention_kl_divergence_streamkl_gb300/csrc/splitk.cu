@@ -281,19 +281,23 @@ __global__ void __launch_bounds__(THREADS)
   }
 }
 
-// One warp merges the S partial states of one (b*h, query) row.
+// One warp merges the S partial states of one (b*h, query) row.  Partial s of
+// row `row` starts at partials + row * row_stride + s * part_stride (floats):
+// [row][split][5] for the Split-K splits, [part][row][5] for key shards.  A part
+// whose keys the row does not see (m = -inf, l = acc = 0) adds nothing.
 __global__ void __launch_bounds__(256) splitk_combine_kernel(const Problem p, int S, const float* __restrict__ partials,
+                                                             long long row_stride, long long part_stride,
                                                              float* __restrict__ out_kl,
                                                              float* __restrict__ out_lse1,
                                                              float* __restrict__ out_lse2) {
   const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= p.BH * p.NQ) return;
-  const float* ps = partials + (size_t)row * S * 5;
+  const float* ps = partials + (size_t)row * row_stride;
   float M1 = kNegInf, M2 = kNegInf;
   for (int s = lane; s < S; s += 32) {
-    M1 = fmaxf(M1, ps[s * 5 + 0]);
-    M2 = fmaxf(M2, ps[s * 5 + 1]);
+    M1 = fmaxf(M1, ps[s * part_stride + 0]);
+    M2 = fmaxf(M2, ps[s * part_stride + 1]);
   }
 #pragma unroll
   for (int m = 16; m >= 1; m >>= 1) {
@@ -302,11 +306,12 @@ __global__ void __launch_bounds__(256) splitk_combine_kernel(const Problem p, in
   }
   float l1 = 0.f, l2 = 0.f, acc = 0.f;
   for (int s = lane; s < S; s += 32) {
-    const float w1 = ex2(ps[s * 5 + 0] - M1);
-    const float w2 = ex2(ps[s * 5 + 1] - M2);
-    l1 = fmaf(ps[s * 5 + 2], w1, l1);
-    acc = fmaf(ps[s * 5 + 4], w1, acc);
-    l2 = fmaf(ps[s * 5 + 3], w2, l2);
+    const float* q = ps + s * part_stride;
+    const float w1 = ex2(q[0] - M1);  // 2^-inf = 0 for a part that saw no key
+    const float w2 = ex2(q[1] - M2);
+    l1 = fmaf(q[2], w1, l1);
+    acc = fmaf(q[4], w1, acc);
+    l2 = fmaf(q[3], w2, l2);
   }
 #pragma unroll
   for (int m = 16; m >= 1; m >>= 1) {
@@ -337,7 +342,8 @@ cudaError_t launch_d(const Problem& p, const void* q1, const void* k1, const voi
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int rows = p.BH * p.NQ;
-  splitk_combine_kernel<<<(rows + 7) / 8, 256, 0, st>>>(p, splits, partials, kl, lse1, lse2);
+  splitk_combine_kernel<<<(rows + 7) / 8, 256, 0, st>>>(p, splits, partials, (long long)splits * 5, 5, kl, lse1,
+                                                        lse2);
   return cudaGetLastError();
 }
 
@@ -388,6 +394,14 @@ int splitk_plan(int BH, int key_tiles, int num_sms) {
     }
   }
   return best;
+}
+
+cudaError_t launch_merge_partials(const Problem& p, int parts, const float* partials, float* kl, float* lse1,
+                                  float* lse2, cudaStream_t st) {
+  const long long rows = (long long)p.BH * p.NQ;
+  if (rows == 0) return cudaSuccess;
+  splitk_combine_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(p, parts, partials, 5, rows * 5, kl, lse1, lse2);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_splitk(const Problem& p, const void* q1, const void* k1, const void* q2, const void* k2,

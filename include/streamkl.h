@@ -149,6 +149,55 @@ streamkl_status streamkl_fwd_splitk_noalloc(const void* q1, const void* k1, cons
                                             float* lse2, void* stream);
 
 /*
+ * Key shards (context parallelism): the keys of a long sequence split into
+ * contiguous ranges, e.g. one per GPU, every range seen by every query row.
+ * (technical summary, 手法 3 "Split-K variant": a key range reduces to five
+ *  scalars per row and ranges merge exactly; the pages split over thread
+ *  blocks, here the same algebra splits over devices.)
+ *
+ * In each of these calls s.NK is the shard's key count and K1, K2 point at the
+ * shard's rows (any strides the shape allows, so a row slice of a larger
+ * [B, H, N, D] tensor is passed as is), which are the keys at global positions
+ * [key_offset, key_offset + s.NK) of a sequence of nk_total keys.  The causal
+ * frontier is the global one: row i keeps global key j iff
+ * j <= i + nk_total - N_Q; rows that see none of the shard's keys are allowed.
+ * Requires 0 <= key_offset, key_offset + s.NK <= nk_total, and, when causal,
+ * N_Q <= nk_total.
+ *
+ * streamkl_fwd_partials: the five scalars of every row over the shard's keys,
+ *   fp32 [B, H, N_Q, 5] = (m1, m2, l1, l2, acc): m_t the reference maximum of
+ *   scale * log2(e) * q_t.k_t, l_t = sum 2^(that - m_t), acc = sum of
+ *   2^(...1 - m1) (q1.k1 - q2.k2) (unscaled).  A row with no visible key gets
+ *   (-inf, -inf, 0, 0, 0).
+ * streamkl_merge_partials: KL, LSE1, LSE2 [B, H, N_Q] from num_parts such
+ *   partial sets stored one after the other, [num_parts][B, H, N_Q, 5] (what
+ *   an all-gather of every shard's partials produces).  Only B, H, N_Q, D and
+ *   the scale of s are used.  Every row must see a key in some part.
+ * streamkl_bwd_keyshard: the backward (setting 1 or 2, as streamkl_bwd_s1 /
+ *   streamkl_bwd_s2) over the shard's keys, given the merged LSE1, LSE2, KL of
+ *   the whole sequence: the shard's dK rows (bf16, K's layout, complete since
+ *   every query row is here) and this shard's unscaled contribution to dQ,
+ *   fp32 [B, H, N_Q, D] contiguous, 16-byte aligned, overwritten.  Summing the
+ *   dq_partial of all shards (an all-reduce) gives the full unscaled dQ.
+ *   Workspace (16-byte aligned) from streamkl_bwd_keyshard_workspace: the fused
+ *   path's fp32 dK rows of one key range.
+ * streamkl_dq_from_partial: bf16 dQ = scale * dq_partial, written with the Q
+ *   strides of s (the full problem's shape).
+ */
+streamkl_status streamkl_fwd_partials(const void* q1, const void* k1, const void* q2, const void* k2,
+                                      streamkl_shape s, long long key_offset, long long nk_total, float* partials,
+                                      void* stream);
+streamkl_status streamkl_merge_partials(const float* partials, int num_parts, streamkl_shape s, float* kl,
+                                        float* lse1, float* lse2, void* stream);
+streamkl_status streamkl_bwd_keyshard_workspace(streamkl_shape s, long long key_offset, long long nk_total,
+                                                size_t* bytes);
+streamkl_status streamkl_bwd_keyshard(int setting, const void* q1, const void* k1, const void* q2, const void* k2,
+                                      streamkl_shape s, long long key_offset, long long nk_total, const float* lse1,
+                                      const float* lse2, const float* kl, const float* g, float* dq_partial,
+                                      void* dk, void* workspace, size_t workspace_bytes, void* stream);
+streamkl_status streamkl_dq_from_partial(const float* dq_partial, streamkl_shape s, void* dq, void* stream);
+
+/*
  * Backward workspace for the current device (0 bytes for the separate path).
  * The fused path adds dK partials with fp32 atomics into an accumulator that
  * the library zeroes; they stay cheap while the rows being accumulated sit in
