@@ -170,10 +170,19 @@ size_t fused_workspace_bytes(const Problem& p, int range_tiles) {
   return bytes;
 }
 
-// AUTO takes the fused path: over key ranges it keeps its atomics in L2 for any
-// N_K.  Every other mode stands as given.
-int resolve_bwd_mode(const Problem&, int mode, size_t, int) {
-  return mode == STREAMKL_BWD_AUTO ? STREAMKL_BWD_FUSED : mode;
+// AUTO takes the fused path (over key ranges it keeps its atomics in L2 for any
+// N_K) unless a head has at most two query tiles and the fused path needs more
+// than one key range: each key tile is then reused by at most two query tiles,
+// so the fused kernel's one visit per tile pair saves little, while its dK
+// atomics and per-range dQ round trips cost more than the separate kernels'
+// recompute (measured: B1 H128 N_Q=128 N_K=64K 3.46 ms separate vs 4.24 fused,
+// B1 H64 N_Q=256 N_K=128K 4.73 vs 5.05; with 4 query tiles, B1 H32 N_Q=512
+// N_K=256K, the fused path wins, 7.19 vs 7.51).  Every other mode stands as given.
+int resolve_bwd_mode(const Problem& p, int mode, size_t l2_bytes, int num_sms) {
+  if (mode != STREAMKL_BWD_AUTO) return mode;
+  const int n_qt = (p.NQ + 127) / 128, n_kt = (p.NK + 127) / 128;
+  if (n_qt <= 2 && fused_range_tiles(p, l2_bytes, num_sms) < n_kt) return STREAMKL_BWD_SEPARATE;
+  return STREAMKL_BWD_FUSED;
 }
 
 streamkl_status device_l2_bytes(size_t* out) {
@@ -421,13 +430,13 @@ streamkl_status streamkl_bwd_workspace(streamkl_shape s, int bwd_mode, size_t* b
   streamkl_status v = validate(s, &p);
   if (v != STREAMKL_OK) return v;
   if (!bytes || bwd_mode < 0 || bwd_mode > STREAMKL_BWD_DK_ONLY) return STREAMKL_ERR_INVALID;
-  bwd_mode = resolve_bwd_mode(p, bwd_mode, 0, 0);
   *bytes = 0;
-  if (bwd_mode == STREAMKL_BWD_FUSED) {
+  if (bwd_mode == STREAMKL_BWD_AUTO || bwd_mode == STREAMKL_BWD_FUSED) {
     size_t l2 = 0;
     int sms = 0;
     if ((v = device_l2_bytes(&l2)) != STREAMKL_OK || (v = device_sms(&sms)) != STREAMKL_OK) return v;
-    *bytes = fused_workspace_bytes(p, fused_range_tiles(p, l2, sms));
+    if (resolve_bwd_mode(p, bwd_mode, l2, sms) == STREAMKL_BWD_FUSED)
+      *bytes = fused_workspace_bytes(p, fused_range_tiles(p, l2, sms));
   }
   return STREAMKL_OK;
 }
@@ -452,14 +461,17 @@ static streamkl_status bwd_common(int setting, const void* q1, const void* k1, c
     return STREAMKL_ERR_INVALID;
   if (want_dq && (!dq || !aligned16(dq))) return STREAMKL_ERR_INVALID;
   if (setting == 2 && !rows_ok(kl)) return STREAMKL_ERR_INVALID;
-  bwd_mode = resolve_bwd_mode(p, bwd_mode, 0, 0);
   int range_tiles = 0;
-  if (bwd_mode == STREAMKL_BWD_FUSED) {
-    if (!workspace || !aligned16(workspace)) return STREAMKL_ERR_WORKSPACE;
+  if (bwd_mode == STREAMKL_BWD_FUSED && (!workspace || !aligned16(workspace))) return STREAMKL_ERR_WORKSPACE;
+  if (bwd_mode == STREAMKL_BWD_AUTO || bwd_mode == STREAMKL_BWD_FUSED) {
     size_t l2 = 0;
     int sms = 0;
     if ((v = device_l2_bytes(&l2)) != STREAMKL_OK || (v = device_sms(&sms)) != STREAMKL_OK) return v;
+    bwd_mode = resolve_bwd_mode(p, bwd_mode, l2, sms);
     range_tiles = fused_range_tiles(p, l2, sms);
+  }
+  if (bwd_mode == STREAMKL_BWD_FUSED) {
+    if (!workspace || !aligned16(workspace)) return STREAMKL_ERR_WORKSPACE;
     if (workspace_bytes < fused_workspace_bytes(p, range_tiles)) return STREAMKL_ERR_WORKSPACE;
   }
   int* status = nullptr;

@@ -79,7 +79,7 @@ typedef struct {
 
 /* Backward path selection (the adaptive rule of section 手法 2 "kernel fusion"). */
 typedef enum {
-  STREAMKL_BWD_AUTO = 0,     /* the fused path (over key ranges when N_K is long; see streamkl_bwd_fused_plan) */
+  STREAMKL_BWD_AUTO = 0,     /* the rule of streamkl_bwd_select */
   STREAMKL_BWD_FUSED = 1,    /* one pass over each QK tile pair, dQ on chip, dK by atomics into fp32 */
   STREAMKL_BWD_SEPARATE = 2, /* a Q-stationary dQ kernel and a K-stationary dK kernel */
   STREAMKL_BWD_DQ_ONLY = 3,  /* separate path, dQ kernel only (dK pointer may be NULL) */
@@ -214,7 +214,13 @@ streamkl_status streamkl_dq_from_partial(const float* dq_partial, streamkl_shape
 streamkl_status streamkl_bwd_workspace(streamkl_shape s, int bwd_mode, size_t* bytes);
 /*
  * Which path AUTO takes (pure host rule, no device; 0 for an invalid shape or
- * num_sms <= 0): the fused path, for every shape.
+ * num_sms <= 0): the fused path (over key ranges when N_K is long; see
+ * streamkl_bwd_fused_plan), except the separate kernels when a head has at
+ * most two 128-row query tiles and the fused path would need more than one key
+ * range -- a key tile is then reused by at most two query tiles, and the
+ * separate kernels' extra recompute costs less than the fused path's dK atomics
+ * and per-range dQ round trips (the "separate kernels under contention" rule of
+ * section 手法 2 "kernel fusion", with the threshold measured on GB300).
  */
 int streamkl_bwd_select(streamkl_shape s, size_t l2_bytes, int num_sms);
 /*

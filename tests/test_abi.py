@@ -179,7 +179,13 @@ def _fused_plan(B, H, NQ, NK, D, l2, sms, causal):
 
 def test_bwd_select_and_fused_plan(lib):
     l2, sms = 135528448, 152  # GB300
-    assert K.bwd_select(1, 8, 524288, 524288, 128, l2, sms) == K.BWD_FUSED  # AUTO is always the fused path
+    assert K.bwd_select(1, 8, 524288, 524288, 128, l2, sms) == K.BWD_FUSED  # many query tiles: fused over ranges
+    assert K.bwd_select(1, 32, 65536, 65536, 128, l2, sms, True) == K.BWD_FUSED
+    # at most two query tiles per head and several key ranges: the separate kernels
+    assert K.bwd_select(1, 128, 128, 65536, 128, l2, sms) == K.BWD_SEPARATE
+    assert K.bwd_select(1, 64, 256, 131072, 128, l2, sms) == K.BWD_SEPARATE
+    assert K.bwd_select(1, 32, 512, 262144, 128, l2, sms) == K.BWD_FUSED  # four query tiles
+    assert K.bwd_select(1, 1, 128, 128, 64, l2, sms) == K.BWD_FUSED  # one key range
     assert K.bwd_select(0, 1, 8, 8, 64, l2, sms) == 0  # invalid shape
     assert K.bwd_select(1, 1, 8, 8, 64, l2, 0) == 0  # no SM count
     # one launch while the live dK rows (heads in flight x N_K x D x 4 B) fit in L2

@@ -222,6 +222,28 @@ def test_b1h8_n524288_causal_setting2():
         del dq, dk
 
 
+def test_auto_takes_separate_kernels_for_short_queries_and_long_keys():
+    """One query tile per head and keys whose live dK rows exceed L2: AUTO picks the separate kernels (the
+    measured rule); both settings against the oracle on four seeded heads."""
+    w = synth.Workload("auto_sep", 1, 32, 128, 65536, 128, False, 0.5, 31)
+    props = torch.cuda.get_device_properties(0)
+    assert skl.bwd_select(w.B, w.H, w.NQ, w.NK, w.D, props.L2_cache_size, props.multi_processor_count,
+                          w.causal) == skl.BWD_SEPARATE
+    assert skl.bwd_workspace_bytes(w.B, w.H, w.NQ, w.NK, w.D, skl.BWD_AUTO, w.causal) == 0
+    inp = synth.make_inputs(w)
+    kl, l1, l2 = _run_fwd(inp, w)
+    rng = np.random.default_rng(4000 + w.seed)
+    heads = [(0, int(x)) for x in sorted(rng.choice(w.H, size=4, replace=False))]
+    for setting in (1, 2):
+        dq, dk = _run_bwd(inp, w, setting, skl.BWD_AUTO, kl, l1, l2)
+        torch.cuda.synchronize()
+        refs = U.map_heads(lambda b, h: U.oracle_head(inp, w, b, h, setting=setting), heads, threads=4)
+        for (b, h), ((rkl, rl1, rl2), (rdq, rdk)) in zip(heads, refs):
+            U.assert_rows(U.np64(kl[b, h]), U.np64(l1[b, h]), U.np64(l2[b, h]), rkl, rl1, rl2, f"head {b},{h}")
+            U.assert_grad(U.np64(dq[b, h]), rdq, f"setting {setting} dQ head {b},{h}")
+            U.assert_grad(U.np64(dk[b, h]), rdk, f"setting {setting} dK head {b},{h}")
+
+
 # ------------------------------------------------------------------ edge cases
 
 @pytest.mark.parametrize("causal", [False, True])
