@@ -313,7 +313,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
       for (int j = 0; j < n_kt; ++j) {
         const int b = j & 1;
-        const bool got = mbar_wait(dk_full + 8 * b, (j >> 1) & 1, status, abort_flag);
+        const bool got = mbar_wait_warp(dk_full + 8 * b, (j >> 1) & 1, status, abort_flag);
         __syncwarp();
         if (!got) break;
         tc_fence_after();
@@ -357,7 +357,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     const uint32_t dsb = sb + L::OFF_DS;
     bool ok = true;
     for (int j = 0; j < n_kt; ++j) {
-      ok = mbar_wait(sa_full, j & 1, status, abort_flag);
+      ok = mbar_wait_warp(sa_full, j & 1, status, abort_flag);
       __syncwarp();
       if (!ok) break;
       tc_fence_after();
@@ -381,7 +381,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           p1_row<false, 32>(held, c, nAr, 0u);
       }
       uint32_t pk[16];
-      ok = mbar_wait(sb_full, j & 1, status, abort_flag);
+      ok = mbar_wait_warp(sb_full, j & 1, status, abort_flag);
       __syncwarp();
       if (!ok) break;
       tc_fence_after();
@@ -416,7 +416,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       reg_fence16(pk);
       // dS smem is free once the dQ and dKp MMAs of the previous tile are done
       if (j >= 1) {
-        ok = mbar_wait(ds_free, (j - 1) & 1, status, abort_flag);
+        ok = mbar_wait_warp(ds_free, (j - 1) & 1, status, abort_flag);
         __syncwarp();
         if (!ok) break;
       }
@@ -432,7 +432,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (lane == 0) mbar_arrive(ds_full);
     }
     // ---- dQ out: group g writes d columns [32g, 32g + 32)
-    const bool done = mbar_wait(all_done, 0, status, abort_flag);
+    const bool done = mbar_wait_warp(all_done, 0, status, abort_flag);
     __syncwarp();
     if (done && grp * 32 < D) {
       tc_fence_after();

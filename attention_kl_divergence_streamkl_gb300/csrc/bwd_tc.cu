@@ -236,7 +236,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     bool ok = true;
     for (int j = 0; j < n_yt; ++j) {
       const int b = j & 1;
-      ok = mbar_wait(s_full, j & 1, status, abort_flag);
+      ok = mbar_wait_warp(s_full, j & 1, status, abort_flag);
       __syncwarp();
       if (!ok) break;
       tc_fence_after();
@@ -271,7 +271,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       reg_fence16(pk);
       // dS buffer b is free once the gradient MMA of tile j - 2 is done
       if (j >= 2) {
-        ok = mbar_wait(ds_free + 8 * b, ((j >> 1) - 1) & 1, status, abort_flag);
+        ok = mbar_wait_warp(ds_free + 8 * b, ((j >> 1) - 1) & 1, status, abort_flag);
         __syncwarp();
         if (!ok) break;
       }
@@ -283,7 +283,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (lane == 0) mbar_arrive(ds_full + 8 * b);
     }
     // ---- G = sum dS Y_opt, scaled, to bf16: group g writes d columns [32g, 32g + 32)
-    const bool got = ok && mbar_wait(g_done, 0, status, abort_flag);
+    const bool got = ok && mbar_wait_warp(g_done, 0, status, abort_flag);
     __syncwarp();
     if (got && grp * 32 < D) {
       tc_fence_after();
@@ -529,7 +529,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     for (int j = 0; j < n_qt; ++j) {
       fetch(j + 1, nA2, nB2, G2);
       const int q = q_begin + j * BQ + r;
-      ok = mbar_wait(sa_full, j & 1, status, abort_flag);
+      ok = mbar_wait_warp(sa_full, j & 1, status, abort_flag);
       __syncwarp();
       if (!ok) break;
       tc_fence_after();
@@ -543,7 +543,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int kg = k0 + grp * 32;
       const bool masked = (kg + 31 >= p.NK) || (q >= p.NQ) || (p.causal && kg + 31 > q + p.off);
       uint32_t pk[16];
-      ok = mbar_wait(sb_full, j & 1, status, abort_flag);
+      ok = mbar_wait_warp(sb_full, j & 1, status, abort_flag);
       __syncwarp();
       if (!ok) break;
       tc_fence_after();
@@ -577,7 +577,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       reg_fence16(pk);
       // dS smem is free once the dK MMA of the previous tile is done
       if (j >= 1) {
-        ok = mbar_wait(ds_free, (j - 1) & 1, status, abort_flag);
+        ok = mbar_wait_warp(ds_free, (j - 1) & 1, status, abort_flag);
         __syncwarp();
         if (!ok) break;
       }
@@ -596,7 +596,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       Gr = G2;
     }
     // ---- dK out: thread = key row k0 + r, group g writes d columns [32g, 32g + 32)
-    const bool got = ok && mbar_wait(g_done, 0, status, abort_flag);
+    const bool got = ok && mbar_wait_warp(g_done, 0, status, abort_flag);
     __syncwarp();
     const int key = k0 + r;
     if (got && grp * 32 < D) {

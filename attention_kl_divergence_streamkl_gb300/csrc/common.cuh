@@ -88,6 +88,14 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* st
   return false;
 }
 
+// The same wait taken by every lane of a warp, with one answer for the whole
+// warp: if any lane gave up, every lane does.  The warp-wide tcgen05
+// instructions that follow such a wait then run on all lanes or on none.
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, int* status,
+                                               volatile int* abort_flag) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, status, abort_flag));
+}
+
 // Drain wait used before a block exits: waits (bounded, ignoring the abort
 // flag) for copies that may still be landing in shared memory.
 constexpr unsigned long long kDrainLimitNs = 100000000ull;

@@ -272,7 +272,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     bool ok = true;
     for (int j = 0; j < n_kt; ++j) {
       const int s = j & 1;
-      const bool got = mbar_wait(bar_sfull + 8 * s, (j >> 1) & 1, status, abort_flag);
+      const bool got = mbar_wait_warp(bar_sfull + 8 * s, (j >> 1) & 1, status, abort_flag);
       __syncwarp();
       if (!got) {
         ok = false;

@@ -253,3 +253,35 @@ def test_binding_reads_views_in_place():
     assert a.is_contiguous() and b.is_contiguous() and st == (H * N * D, N * D, D)
     g = K._grad_like(qkv[:, :, 0].permute(0, 2, 1, 3), (N * 3 * H * D, D, 3 * H * D), N)
     assert g.stride() == (N * 3 * H * D, D, 3 * H * D, 1)
+
+
+def test_key_shard_entry_points_validate_before_any_launch(lib):
+    """streamkl_fwd_partials / _bwd_keyshard / _merge_partials / _dq_from_partial reject bad shards and
+    pointers synchronously (no device is touched on these paths)."""
+    p = [fake_ptr(64 * i) for i in range(16)]
+    s = K.make_shape(1, 2, 64, 32, 64, None, True)  # a 32-key shard of a longer sequence
+    part = fake_ptr(1 << 12)
+    # the shard must lie inside the sequence
+    assert lib.streamkl_fwd_partials(p[0], p[1], p[2], p[3], s, -1, 128, part, None) == K.ERR_INVALID
+    assert lib.streamkl_fwd_partials(p[0], p[1], p[2], p[3], s, 100, 128, part, None) == K.ERR_INVALID
+    # causal needs N_Q <= nk_total (here 64 > 48), not N_Q <= the shard's keys
+    assert lib.streamkl_fwd_partials(p[0], p[1], p[2], p[3], s, 16, 48, part, None) == K.ERR_INVALID
+    assert lib.streamkl_fwd_partials(p[0], p[1], p[2], p[3], s, 0, 64, fake_ptr(2), None) == K.ERR_INVALID
+    assert lib.streamkl_fwd_partials(None, p[1], p[2], p[3], s, 0, 64, part, None) == K.ERR_INVALID
+    s0 = K.make_shape(1, 2, 0, 32, 64)
+    assert lib.streamkl_fwd_partials(None, None, None, None, s0, 0, 64, None, None) == K.OK  # no rows: no-op
+    # merge: at least one part, aligned rows
+    sm = K.make_shape(1, 2, 64, 1, 64)
+    assert lib.streamkl_merge_partials(part, 0, sm, p[4], p[5], p[6], None) == K.ERR_INVALID
+    assert lib.streamkl_merge_partials(part, 2, sm, fake_ptr(1), p[5], p[6], None) == K.ERR_INVALID
+    # backward on a shard: setting, dK, dQ-partial and workspace checks come first
+    args = (p[0], p[1], p[2], p[3], s, 0, 64, p[4], p[5], p[6], p[7])
+    assert lib.streamkl_bwd_keyshard(3, *args, p[8], p[9], p[10], 1 << 20, None) == K.ERR_INVALID
+    assert lib.streamkl_bwd_keyshard(1, *args, p[8], fake_ptr(2), p[10], 1 << 20, None) == K.ERR_INVALID
+    assert lib.streamkl_bwd_keyshard(1, *args, fake_ptr(4), p[9], p[10], 1 << 20, None) == K.ERR_INVALID
+    assert lib.streamkl_bwd_keyshard(1, *args, p[8], p[9], None, 0, None) == K.ERR_WORKSPACE
+    assert lib.streamkl_bwd_keyshard(2, p[0], p[1], p[2], p[3], s, 0, 64, p[4], p[5], None, p[7], p[8], p[9],
+                                     p[10], 1 << 20, None) == K.ERR_INVALID  # setting 2 needs the merged KL
+    # dQ from the summed partials: aligned buffers
+    assert lib.streamkl_dq_from_partial(fake_ptr(4), sm, p[9], None) == K.ERR_INVALID
+    assert lib.streamkl_dq_from_partial(p[8], sm, fake_ptr(2), None) == K.ERR_INVALID
