@@ -102,3 +102,28 @@ def test_invalid_shard_arguments_are_refused():
         skl.fwd_partials(q1, k1, q2, k2, -1, 128)
     with pytest.raises(skl.StreamKLError):
         skl.fwd_partials(q1, k1[:, :, :32], q2, k2[:, :, :32], 0, 32, None, True)  # causal with N_Q > nk_total
+
+
+def test_shard_module_on_one_gpu():
+    """shard.py's head and key paths with a world of one (no process group): the library's kernels behind
+    every call, against the unsharded calls."""
+    from attention_kl_divergence_streamkl_gb300 import shard
+    w = synth.Workload("shardmod", 1, 4, 256, 640, 128, True, 0.5, 91)
+    inp = synth.make_inputs(w)
+    q1, k1, q2, k2 = U.dev_inputs(inp)
+    g = torch.from_numpy(inp["g"]).cuda()
+    sc = w.softmax_scale
+    kl, l1, l2 = skl.fwd(q1, k1, q2, k2, sc, True)
+    hkl, hl1, hl2, loss = shard.heads_forward(q1, k1, q2, k2, sc, True, g)
+    assert torch.equal(hkl, kl) and abs(float(loss) - float((g.double() * kl.double()).sum())) < 1e-9
+    k1l, k0 = shard.local_keys(k1)
+    k2l, _ = shard.local_keys(k2)
+    assert (k0, k1l.shape[2]) == (0, w.NK)
+    skl_, sl1, sl2 = shard.keys_forward(q1, k1l, q2, k2l, k0, w.NK, sc, True)
+    assert float((skl_ - kl).abs().max()) < 2e-4 and float((sl1 - l1).abs().max()) < 2e-5
+    for setting in (1, 2):
+        dq, dk = shard.keys_backward(setting, q1, k1l, q2, k2l, k0, w.NK, sl1, sl2, skl_, g, sc, True)
+        rq, rk = (skl.bwd_s1(q1, k1, q2, k2, l1, l2, g, sc, True, skl.BWD_FUSED) if setting == 1 else
+                  skl.bwd_s2(q1, k1, q2, k2, l1, l2, kl, g, sc, True, skl.BWD_FUSED))
+        U.assert_grad(U.np64(dq), U.np64(rq), f"setting {setting} dQ via shard.py")
+        U.assert_grad(U.np64(dk), U.np64(rk), f"setting {setting} dK via shard.py")
