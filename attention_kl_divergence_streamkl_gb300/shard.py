@@ -140,6 +140,47 @@ def keys_backward(setting, q1, k1, q2, k2, key_offset: int, nk_total: int, lse1,
     return ops.dq_from_partial(dq_part, q1 if setting == 2 else q2, scale), dk
 
 
+class _KeyShardedKL(torch.autograd.Function):
+    """KL per row of the whole sequence from this rank's key shard, differentiable (see keys_attention_kl)."""
+
+    @staticmethod
+    def forward(ctx, q1, k1, q2, k2, key_offset, nk_total, scale, causal, group, ops):
+        kl, lse1, lse2 = keys_forward(q1, k1, q2, k2, key_offset, nk_total, scale, causal, group, ops)
+        ctx.save_for_backward(q1, k1, q2, k2, kl, lse1, lse2)
+        ctx.args = (key_offset, nk_total, scale, causal, group, ops)
+        return kl
+
+    @staticmethod
+    def backward(ctx, grad_kl):
+        q1, k1, q2, k2, kl, lse1, lse2 = ctx.saved_tensors
+        key_offset, nk_total, scale, causal, group, ops = ctx.args
+        g = grad_kl.contiguous().to(kl.dtype)
+        dq1 = dk1 = dq2 = dk2 = None
+        if ctx.needs_input_grad[2] or ctx.needs_input_grad[3]:
+            dq2, dk2 = keys_backward(1, q1, k1, q2, k2, key_offset, nk_total, lse1, lse2, kl, g, scale, causal,
+                                     group, ops)
+        if ctx.needs_input_grad[0] or ctx.needs_input_grad[1]:
+            dq1, dk1 = keys_backward(2, q1, k1, q2, k2, key_offset, nk_total, lse1, lse2, kl, g, scale, causal,
+                                     group, ops)
+        return dq1, dk1, dq2, dk2, None, None, None, None, None, None
+
+
+def keys_attention_kl(q1, k1, q2, k2, key_offset: int, nk_total: int, scale=None, causal=False, group=None,
+                      ops=DEFAULT_OPS):
+    """Differentiable per-row KL [B, H, N_Q] of the whole sequence, computed from this rank's key shard.
+
+    Every rank holds every query row (q_t replicated) and its own keys; every
+    rank gets the same KL.  In the backward, the gradient of q_t is the whole
+    dQ (the shards' contributions all-reduced, so replicated queries need no
+    further reduction) and the gradient of k_t covers this rank's keys.  The
+    upstream gradient must be the same on every rank, as it is for a loss
+    computed from the returned KL on each rank.  Heads need no such function:
+    with the heads split over ranks, attention_kl on each rank's heads gives
+    that rank's gradients, and the job's loss is the all-reduced sum.
+    """
+    return _KeyShardedKL.apply(q1, k1, q2, k2, key_offset, nk_total, scale, causal, group, ops)
+
+
 def mean_rows_grad(B: int, H: int, NQ: int, device=None, dtype=torch.float32) -> torch.Tensor:
     """g for a loss that is the mean of KL over all B * H * N_Q rows of the job."""
     return torch.full((B, H, NQ), 1.0 / max(B * H * NQ, 1), dtype=dtype, device=device)
@@ -158,4 +199,4 @@ def local_keys(t: torch.Tensor, group=None, align: int = 128) -> tuple[torch.Ten
 
 
 __all__ = ["split_range", "head_range", "heads_forward", "heads_backward", "key_range", "keys_forward",
-           "keys_backward", "mean_rows_grad", "local_heads", "local_keys", "DEFAULT_OPS"]
+           "keys_backward", "keys_attention_kl", "mean_rows_grad", "local_heads", "local_keys", "DEFAULT_OPS"]

@@ -127,3 +127,21 @@ def test_shard_module_on_one_gpu():
                   skl.bwd_s2(q1, k1, q2, k2, l1, l2, kl, g, sc, True, skl.BWD_FUSED))
         U.assert_grad(U.np64(dq), U.np64(rq), f"setting {setting} dQ via shard.py")
         U.assert_grad(U.np64(dk), U.np64(rk), f"setting {setting} dK via shard.py")
+
+
+def test_key_sharded_autograd_on_one_gpu():
+    """keys_attention_kl with a world of one equals attention_kl: values and the gradients of all four inputs."""
+    from attention_kl_divergence_streamkl_gb300 import shard
+    w = synth.Workload("shardgrad", 1, 2, 200, 384, 64, True, 0.5, 92)
+    inp = synth.make_inputs(w)
+    base = U.dev_inputs(inp)
+    a = [t.clone().requires_grad_() for t in base]
+    b = [t.clone().requires_grad_() for t in base]
+    la = skl.attention_kl(*a, w.softmax_scale, True, "mean")
+    la.backward()
+    kl = shard.keys_attention_kl(*b, 0, w.NK, w.softmax_scale, True)
+    lb = kl.mean()
+    lb.backward()
+    assert abs(float(la) - float(lb)) < 1e-5
+    for x, y, name in zip(a, b, ("q1", "k1", "q2", "k2")):
+        U.assert_grad(U.np64(y.grad), U.np64(x.grad), f"{name} grad via keys_attention_kl")

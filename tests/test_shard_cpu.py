@@ -72,6 +72,12 @@ def _rank(rank, world, port, out):
             grads[setting] = shard.keys_backward(setting, t["q1"], k1l, t["q2"], k2l, k0, w.NK, l1, l2, kl, g, sc,
                                                  causal, ops=OPS)
         res[("keys", causal)] = ((k0, k0 + k1l.shape[2]), (kl, l1, l2), grads)
+        # ---- the differentiable form: mean KL over all rows, gradients of every input
+        ins = [t["q1"].clone().requires_grad_(), k1l.clone().requires_grad_(), t["q2"].clone().requires_grad_(),
+               k2l.clone().requires_grad_()]
+        kl = shard.keys_attention_kl(*ins, k0, w.NK, sc, causal, ops=OPS)
+        kl.mean().backward()
+        res[("autograd", causal)] = (float(kl.mean()), [x.grad.clone() for x in ins])
     out[rank] = res
     dist.barrier()
     dist.destroy_process_group()
@@ -112,3 +118,13 @@ def test_two_gloo_ranks_shard_heads_and_keys():
                 assert np.allclose(dq.numpy(), ref[s][0], atol=1e-12)
                 assert np.allclose(dk.numpy(), ref[s][1][:, :, k0:k1], atol=1e-12)
         assert ranges == [(0, 32), (32, 70)]
+        # autograd: g = 1 / (B H N_Q) per row; setting 2 gives the teacher's, setting 1 the student's gradients
+        gm = np.full((w.B, w.H, w.NQ), 1.0 / (w.B * w.H * w.NQ))
+        r1 = O.backward(1, f["q1"], f["k1"], f["q2"], f["k2"], sc, causal, gm)
+        r2 = O.backward(2, f["q1"], f["k1"], f["q2"], f["k2"], sc, causal, gm)
+        for r, (k0, k1) in enumerate(ranges):
+            loss, (gq1, gk1, gq2, gk2) = out[r][("autograd", causal)]
+            assert loss == pytest.approx(float(rkl.mean()), rel=1e-12)
+            assert np.allclose(gq1.numpy(), r2[0], atol=1e-12) and np.allclose(gq2.numpy(), r1[0], atol=1e-12)
+            assert np.allclose(gk1.numpy(), r2[1][:, :, k0:k1], atol=1e-12)
+            assert np.allclose(gk2.numpy(), r1[1][:, :, k0:k1], atol=1e-12)
