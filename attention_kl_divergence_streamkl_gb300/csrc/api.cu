@@ -378,7 +378,7 @@ streamkl_status streamkl_bwd_keyshard(int setting, const void* q1, const void* k
   if (setting != 1 && setting != 2) return STREAMKL_ERR_INVALID;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (!dk || !aligned16(dk)) return STREAMKL_ERR_INVALID;
-  if (p.NQ == 0) return from_cuda(cudaMemsetAsync(dk, 0, (size_t)p.BH * p.NK * p.D * 2, st));
+  if (p.NQ == 0) return from_cuda(launch_zero_k_rows(p, dk, st));
   if (!inputs_ok(q1, k1, q2, k2) || !rows_ok(lse1) || !rows_ok(lse2) || !rows_ok(g)) return STREAMKL_ERR_INVALID;
   if (setting == 2 && !rows_ok(kl)) return STREAMKL_ERR_INVALID;
   if (!dq_partial || !aligned16(dq_partial)) return STREAMKL_ERR_INVALID;
@@ -454,8 +454,8 @@ static streamkl_status bwd_common(int setting, const void* q1, const void* k1, c
   const bool want_dk = bwd_mode != STREAMKL_BWD_DQ_ONLY;
   if (want_dk && (!dk || !aligned16(dk))) return STREAMKL_ERR_INVALID;
   if (p.NQ == 0) {
-    // no query rows: the loss is an empty sum, so dK is zero
-    return want_dk ? from_cuda(cudaMemsetAsync(dk, 0, (size_t)p.BH * p.NK * p.D * 2, st)) : STREAMKL_OK;
+    // no query rows: the loss is an empty sum, so dK is zero (written with dK's strides)
+    return want_dk ? from_cuda(launch_zero_k_rows(p, dk, st)) : STREAMKL_OK;
   }
   if (!inputs_ok(q1, k1, q2, k2) || !rows_ok(lse1) || !rows_ok(lse2) || !rows_ok(g))
     return STREAMKL_ERR_INVALID;

@@ -578,6 +578,34 @@ cudaError_t launch_bwd_fused(const Problem& p, int setting, const BwdIn& in, voi
   return fused_d<128>(p, setting, in, dq, dk, workspace, range_tiles, status, st, dq_f32);
 }
 
+// Zeroes rows [0, nrows) of every head of a bf16 [B, H, N, D] view with strides (sb, sh, sn): one thread
+// writes 8 values.
+template <int D>
+__global__ void __launch_bounds__(256)
+    zero_rows_kernel(__nv_bfloat16* __restrict__ out, const int H, const int nrows, const long long sb,
+                     const long long sh, const long long sn, const size_t n8) {
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += (size_t)gridDim.x * blockDim.x) {
+    const size_t rr = i / (D / 8);
+    const int d = (int)(i % (D / 8)) * 8;
+    const int bh = (int)(rr / (size_t)nrows), r = (int)(rr % (size_t)nrows);
+    *reinterpret_cast<uint4*>(out + row_offset(bh, H, r, sb, sh, sn) + d) = make_uint4(0, 0, 0, 0);
+  }
+}
+
+template <int D>
+cudaError_t zero_k_rows(const Problem& p, void* dk, cudaStream_t st) {
+  const size_t n8 = (size_t)p.BH * p.NK * (D / 8);
+  if (n8 == 0) return cudaSuccess;
+  const int blocks = (int)((n8 + 255) / 256 < 4096 ? (n8 + 255) / 256 : 4096);
+  zero_rows_kernel<D><<<blocks, 256, 0, st>>>(static_cast<__nv_bfloat16*>(dk), p.H, p.NK, p.ks_b, p.ks_h, p.ks_n,
+                                             n8);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_zero_k_rows(const Problem& p, void* dk, cudaStream_t st) {
+  return p.D == 64 ? zero_k_rows<64>(p, dk, st) : zero_k_rows<128>(p, dk, st);
+}
+
 cudaError_t launch_rows_to_bf16(const Problem& p, const float* acc, void* out, cudaStream_t st) {
   if (p.D == 64) return convert_rows<64>(acc, out, p, p.NQ, 0, p.NQ, p.qs_b, p.qs_h, p.qs_n, st);
   return convert_rows<128>(acc, out, p, p.NQ, 0, p.NQ, p.qs_b, p.qs_h, p.qs_n, st);

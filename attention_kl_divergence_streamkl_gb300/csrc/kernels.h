@@ -77,6 +77,8 @@ cudaError_t launch_bwd_separate(const Problem& p, int setting, const BwdIn& in, 
 // workspace holds only the dK rows of one range.
 cudaError_t launch_bwd_fused(const Problem& p, int setting, const BwdIn& in, void* dq, void* dk, float* workspace,
                              int range_tiles, int* status, cudaStream_t st, float* dq_f32 = nullptr);
+// dK = 0 for every key row of every head, written with K's strides (a backward with no query rows).
+cudaError_t launch_zero_k_rows(const Problem& p, void* dk, cudaStream_t st);
 // out row n of head bh = bf16(scale * acc[bh][n]) for n < N_Q, with Q's strides.
 cudaError_t launch_rows_to_bf16(const Problem& p, const float* acc, void* out, cudaStream_t st);
 // First 128-query tile whose rows see key k0.

@@ -69,7 +69,11 @@ def heads_forward(q1, k1, q2, k2, scale=None, causal=False, g=None, group=None, 
     Returns (kl, lse1, lse2, loss): the local per-row values and the sum over
     every rank of sum_i g_i KL_i (g = 1 per row when None), all-reduced.
     """
-    kl, lse1, lse2 = ops.fwd(q1, k1, q2, k2, scale, causal)
+    B, Hl, NQ, _ = q1.shape
+    if Hl == 0:  # more ranks than heads: this rank owns none, but still joins the all-reduce
+        kl, lse1, lse2 = (torch.zeros((B, 0, NQ), dtype=torch.float32, device=q1.device) for _ in range(3))
+    else:
+        kl, lse1, lse2 = ops.fwd(q1, k1, q2, k2, scale, causal)
     w = torch.ones_like(kl) if g is None else g
     loss = (w.double() * kl.double()).sum().reshape(1)
     if _world(group)[0] > 1:
@@ -80,6 +84,9 @@ def heads_forward(q1, k1, q2, k2, scale=None, causal=False, g=None, group=None, 
 def heads_backward(setting, q1, k1, q2, k2, lse1, lse2, kl, g, scale=None, causal=False, ops=DEFAULT_OPS,
                    bwd_mode=_lib.BWD_AUTO):
     """Backward on this rank's heads: no exchange (each head's gradient is local)."""
+    if q1.shape[1] == 0:  # a rank that owns no heads
+        q, k = (q2, k2) if setting == 1 else (q1, k1)
+        return torch.empty_like(q), torch.empty_like(k)
     if setting == 1:
         return ops.bwd_s1(q1, k1, q2, k2, lse1, lse2, g, scale, causal, bwd_mode)
     return ops.bwd_s2(q1, k1, q2, k2, lse1, lse2, kl, g, scale, causal, bwd_mode)

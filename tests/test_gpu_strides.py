@@ -175,3 +175,35 @@ def test_unaligned_view_is_copied_not_refused():
     b = skl.fwd(*contig, w.softmax_scale, False)
     for x, y in zip(a, b):
         assert torch.equal(x, y)
+
+
+@pytest.mark.parametrize("mode", [K.BWD_FUSED, K.BWD_SEPARATE])
+def test_no_query_rows_zero_only_the_strided_dk_rows(mode):
+    """With N_Q = 0 the loss is an empty sum, so dK is zero: it is written with
+    K's strides into slot 1 of a packed gradient buffer, and slots 0 and 2 keep
+    their sentinel."""
+    B, H, NK, D = 2, 3, 200, 128
+    w = synth.Workload("packed_empty", B, H, 0, NK, D, True, 0.5, 98)
+    inp = synth.make_inputs(w)
+    q1, k1, q2, k2 = U.dev_inputs(inp)
+    pad = torch.zeros_like(k1)
+    _, k1p, _ = packed([pad, k1, pad])
+    _, k2p, _ = packed([pad, k2, pad])
+    sentinel = torch.tensor(-7.0, dtype=torch.bfloat16).item()
+    grad = torch.full((B, NK, 3, H, D), sentinel, dtype=torch.bfloat16, device="cuda")
+    dk_v = grad[:, :, 1].permute(0, 2, 1, 3)
+    ks = K._bhn_strides(k2p)
+    assert ks == K._bhn_strides(dk_v)
+    s = K.make_shape(B, H, 0, NK, D, w.softmax_scale, True, (0, 0, 0), ks)
+    nbytes = ctypes.c_size_t(0)
+    assert K.lib().streamkl_bwd_workspace(s, mode, ctypes.byref(nbytes)) == K.OK
+    ws = torch.empty(max(16, nbytes.value), dtype=torch.uint8, device="cuda")
+    rows = torch.zeros((B, H, 16), device="cuda")  # 16-byte aligned stand-ins for the empty row vectors
+    dq = torch.empty((B, H, 0, D), dtype=torch.bfloat16, device="cuda")
+    st = K.lib().streamkl_bwd_s1(K._ptr(q1), K._ptr(k1p), K._ptr(q2), K._ptr(k2p), s, K._ptr(rows), K._ptr(rows),
+                                 K._ptr(rows), K._ptr(dq), K._ptr(dk_v), mode, K._ptr(ws), nbytes.value,
+                                 K._stream(k1.device))
+    assert st == K.OK
+    torch.cuda.synchronize()
+    assert bool((dk_v == 0).all())
+    assert bool((grad[:, :, 0] == sentinel).all()) and bool((grad[:, :, 2] == sentinel).all())

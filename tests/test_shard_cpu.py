@@ -128,3 +128,22 @@ def test_two_gloo_ranks_shard_heads_and_keys():
             assert np.allclose(gq1.numpy(), r2[0], atol=1e-12) and np.allclose(gq2.numpy(), r1[0], atol=1e-12)
             assert np.allclose(gk1.numpy(), r2[1][:, :, k0:k1], atol=1e-12)
             assert np.allclose(gk2.numpy(), r1[1][:, :, k0:k1], atol=1e-12)
+
+
+def test_a_rank_without_heads_calls_no_kernel():
+    """More ranks than heads leaves a rank an empty head range; it returns empty
+    values and gradients without calling the kernels (which refuse H = 0)."""
+    import types
+
+    def refuse(*a, **k):
+        raise AssertionError("kernel called for an empty head range")
+
+    ops = types.SimpleNamespace(fwd=refuse, bwd_s1=refuse, bwd_s2=refuse)
+    assert shard.split_range(1, 2, 0) == (0, 0)
+    q = torch.zeros((2, 0, 5, 8))
+    k = torch.zeros((2, 0, 7, 8))
+    kl, l1, l2, loss = shard.heads_forward(q, k, q, k, 0.5, False, ops=ops)
+    assert kl.shape == (2, 0, 5) and l1.shape == (2, 0, 5) and float(loss) == 0.0
+    for setting in (1, 2):
+        dq, dk = shard.heads_backward(setting, q, k, q, k, l1, l2, kl, kl, 0.5, False, ops=ops)
+        assert dq.shape == q.shape and dk.shape == k.shape
