@@ -65,6 +65,9 @@ SIGNATURES = {
     "streamkl_bwd_fused_plan": (_I, [Shape, _SZ, _I, ctypes.POINTER(_I), ctypes.POINTER(_SZ)]),
     "streamkl_bwd_s1": (_I, [_P, _P, _P, _P, Shape, _F, _F, _F, _P, _P, _I, _P, _SZ, _S]),
     "streamkl_bwd_s2": (_I, [_P, _P, _P, _P, Shape, _F, _F, _F, _F, _P, _P, _I, _P, _SZ, _S]),
+    "streamkl_bwd_mutual": (_I, [_P, _P, _P, _P, Shape, _F, _F, _F, _F, _P, _P, _P, _P, _I, _P, _SZ, _S]),
+    "streamkl_bwd_mutual_select": (_I, [Shape, _SZ, _I]),
+    "streamkl_bwd_mutual_workspace": (_I, [Shape, _I, ctypes.POINTER(_SZ)]),
     "streamkl_status_string": (ctypes.c_char_p, [_I]),
     "streamkl_check_device_status": (_I, [_S]),
     "streamkl_debug_wait_timeout": (_I, [_I, _S]),
@@ -355,6 +358,39 @@ def bwd_s1(q1, k1, q2, k2, lse1, lse2, g, scale=None, causal=False, bwd_mode=BWD
 def bwd_s2(q1, k1, q2, k2, lse1, lse2, kl, g, scale=None, causal=False, bwd_mode=BWD_AUTO):
     """Setting 2 (P2 fixed): (dQ1, dK1) bf16."""
     return _bwd(2, q1, k1, q2, k2, lse1, lse2, kl, g, scale, causal, bwd_mode)
+
+
+def bwd_mutual_select(B, H, NQ, NK, D, l2_bytes, num_sms, causal=False) -> int:
+    """AUTO's path for the mutual case (BWD_SEPARATE = the mutual kernels, BWD_FUSED = a fused pass per setting)."""
+    return lib().streamkl_bwd_mutual_select(make_shape(B, H, NQ, NK, D, None, causal), int(l2_bytes), int(num_sms))
+
+
+def bwd_mutual(q1, k1, q2, k2, lse1, lse2, kl, g, scale=None, causal=False, bwd_mode=BWD_AUTO):
+    """Gradients of all four inputs (the mutual case): (dQ1, dK1, dQ2, dK2) bf16.
+
+    bwd_mode BWD_SEPARATE rebuilds each logit tile pair once for both settings;
+    BWD_FUSED runs one fused pass per setting; BWD_AUTO picks by shape.
+    """
+    (q1, k1, q2, k2), host, qs, ks = _prep(q1, k1, q2, k2)
+    B, H, NQ, D = q1.shape
+    NK = k1.shape[2]
+    dev = q1.device
+    s = make_shape(B, H, NQ, NK, D, scale, causal, qs, ks)
+    lse1 = _rows(lse1, dev, (B, H, NQ), "lse1")
+    lse2 = _rows(lse2, dev, (B, H, NQ), "lse2")
+    kl = _rows(kl, dev, (B, H, NQ), "kl")
+    g = _rows(g, dev, (B, H, NQ), "g")
+    nbytes = ctypes.c_size_t(0)
+    _check(lib().streamkl_bwd_mutual_workspace(s, int(bwd_mode), ctypes.byref(nbytes)),
+           "streamkl_bwd_mutual_workspace")
+    ws = torch.empty(max(16, nbytes.value), dtype=torch.uint8, device=dev)
+    dq1, dq2 = _grad_like(q1, qs, NQ), _grad_like(q2, qs, NQ)
+    dk1, dk2 = _grad_like(k1, ks, NK), _grad_like(k2, ks, NK)
+    _check(lib().streamkl_bwd_mutual(_ptr(q1), _ptr(k1), _ptr(q2), _ptr(k2), s, _ptr(lse1), _ptr(lse2), _ptr(kl),
+                                     _ptr(g), _ptr(dq1), _ptr(dk1), _ptr(dq2), _ptr(dk2), int(bwd_mode), _ptr(ws),
+                                     nbytes.value, _stream(dev)),
+           "streamkl_bwd_mutual")
+    return _back((dq1, dk1, dq2, dk2), host)
 
 
 def check_device_status(device=None) -> int:

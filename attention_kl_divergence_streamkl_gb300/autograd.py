@@ -5,7 +5,9 @@ or sum) with P_t = softmax(scale Q_t K_t^T).  The forward is streamkl_fwd; the
 backward calls the recompute backward of the StreamKL technical summary
 (gist.science/ja/paper/2606.20005, section 手法 2) in whichever settings the
 inputs need: setting 1 (P1 held fixed) for gradients of Q2/K2, setting 2 (P2
-held fixed) for gradients of Q1/K1, both when both sides require grad.  Only
+held fixed) for gradients of Q1/K1, both when both sides require grad (in one
+call, which rebuilds each logit tile pair once for both settings where that is
+faster).  Only
 the reduction of the per-row values to a scalar happens in PyTorch.
 """
 from __future__ import annotations
@@ -36,6 +38,10 @@ class _AttentionKL(torch.autograd.Function):
         need1 = ctx.needs_input_grad[0] or ctx.needs_input_grad[1]
         need2 = ctx.needs_input_grad[2] or ctx.needs_input_grad[3]
         dq1 = dk1 = dq2 = dk2 = None
+        if need1 and need2 and ctx.bwd_mode in (_lib.BWD_AUTO, _lib.BWD_FUSED, _lib.BWD_SEPARATE):
+            # the mutual case in one call (the library picks one recompute for both settings, or a pass each)
+            return (*_lib.bwd_mutual(q1, k1, q2, k2, lse1, lse2, kl, g, ctx.scale, ctx.causal, ctx.bwd_mode),
+                    None, None, None, None)
         if need2:
             dq2, dk2 = _lib.bwd_s1(q1, k1, q2, k2, lse1, lse2, g, ctx.scale, ctx.causal, ctx.bwd_mode)
         if need1:

@@ -185,6 +185,27 @@ int resolve_bwd_mode(const Problem& p, int mode, size_t l2_bytes, int num_sms) {
   return STREAMKL_BWD_FUSED;
 }
 
+// The mutual case (both settings' gradients): AUTO takes the mutual kernels
+// (one recompute of each logit tile pair for both settings, reported as
+// STREAMKL_BWD_SEPARATE) when the fused path would run over several key ranges
+// and a head has at most kMutualMaxQTiles query tiles; there every key tile is
+// reused by few query tiles, and the fused path's dK atomics and per-range dQ
+// round trips, paid twice, outweigh the mutual kernels' second recompute
+// (measured, ms for both settings' backward, non-causal N_K = 64K: B1 H32
+// N_Q=128 2.07 mutual, 3.52 two fused passes, 2.84 two separate passes; B1 H8
+// N_Q=1024 1.84, 2.50, 2.43; N_Q=2048 2.36, 2.54, 3.13; N_Q=4096 4.54, 4.71,
+// 5.96 -- the gain shrinks as query tiles grow).  Otherwise one fused pass per
+// setting, which wins when the fused path keeps all keys in one range (B1 H8
+// N64K causal 32.3 mutual against 30.3; B1 H8 N16K causal 2.23 against 2.10;
+// B2 H32 N4096 non-causal 2.28 against 2.18, causal 1.29 against 1.30).
+constexpr int kMutualMaxQTiles = 16;
+int resolve_mutual_mode(const Problem& p, int mode, size_t l2_bytes, int num_sms) {
+  if (mode != STREAMKL_BWD_AUTO) return mode;
+  const int n_qt = (p.NQ + 127) / 128, n_kt = (p.NK + 127) / 128;
+  if (n_qt <= kMutualMaxQTiles && fused_range_tiles(p, l2_bytes, num_sms) < n_kt) return STREAMKL_BWD_SEPARATE;
+  return STREAMKL_BWD_FUSED;
+}
+
 streamkl_status device_l2_bytes(size_t* out) {
   int dev = 0, l2 = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return STREAMKL_ERR_CUDA;
@@ -494,6 +515,71 @@ streamkl_status streamkl_bwd_s2(const void* q1, const void* k1, const void* q2, 
                                 const float* lse1, const float* lse2, const float* kl, const float* g, void* dq1,
                                 void* dk1, int bwd_mode, void* workspace, size_t workspace_bytes, void* stream) {
   return bwd_common(2, q1, k1, q2, k2, s, lse1, lse2, kl, g, dq1, dk1, bwd_mode, workspace, workspace_bytes, stream);
+}
+
+int streamkl_bwd_mutual_select(streamkl_shape s, size_t l2_bytes, int num_sms) {
+  Problem p;
+  if (validate(s, &p) != STREAMKL_OK || num_sms <= 0) return 0;
+  return resolve_mutual_mode(p, STREAMKL_BWD_AUTO, l2_bytes, num_sms);
+}
+
+static bool mutual_mode_ok(int mode) {
+  return mode == STREAMKL_BWD_AUTO || mode == STREAMKL_BWD_FUSED || mode == STREAMKL_BWD_SEPARATE;
+}
+
+streamkl_status streamkl_bwd_mutual_workspace(streamkl_shape s, int bwd_mode, size_t* bytes) {
+  Problem p;
+  streamkl_status v = validate(s, &p);
+  if (v != STREAMKL_OK) return v;
+  if (!bytes || !mutual_mode_ok(bwd_mode)) return STREAMKL_ERR_INVALID;
+  *bytes = 0;
+  if (bwd_mode == STREAMKL_BWD_SEPARATE) return STREAMKL_OK;
+  size_t l2 = 0;
+  int sms = 0;
+  if ((v = device_l2_bytes(&l2)) != STREAMKL_OK || (v = device_sms(&sms)) != STREAMKL_OK) return v;
+  if (resolve_mutual_mode(p, bwd_mode, l2, sms) == STREAMKL_BWD_FUSED)
+    *bytes = fused_workspace_bytes(p, fused_range_tiles(p, l2, sms));
+  return STREAMKL_OK;
+}
+
+streamkl_status streamkl_bwd_mutual(const void* q1, const void* k1, const void* q2, const void* k2,
+                                    streamkl_shape s, const float* lse1, const float* lse2, const float* kl,
+                                    const float* g, void* dq1, void* dk1, void* dq2, void* dk2, int bwd_mode,
+                                    void* workspace, size_t workspace_bytes, void* stream) {
+  Problem p;
+  streamkl_status v = validate(s, &p);
+  if (v != STREAMKL_OK) return v;
+  if (!mutual_mode_ok(bwd_mode)) return STREAMKL_ERR_INVALID;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (!dk1 || !aligned16(dk1) || !dk2 || !aligned16(dk2)) return STREAMKL_ERR_INVALID;
+  if (p.NQ == 0) {  // an empty sum: both dK are zero
+    cudaError_t e = launch_zero_k_rows(p, dk1, st);
+    return from_cuda(e != cudaSuccess ? e : launch_zero_k_rows(p, dk2, st));
+  }
+  if (!inputs_ok(q1, k1, q2, k2) || !rows_ok(lse1) || !rows_ok(lse2) || !rows_ok(kl) || !rows_ok(g))
+    return STREAMKL_ERR_INVALID;
+  if (!dq1 || !aligned16(dq1) || !dq2 || !aligned16(dq2)) return STREAMKL_ERR_INVALID;
+  if (bwd_mode == STREAMKL_BWD_FUSED && (!workspace || !aligned16(workspace))) return STREAMKL_ERR_WORKSPACE;
+  int range_tiles = 0;
+  if (bwd_mode != STREAMKL_BWD_SEPARATE) {
+    size_t l2 = 0;
+    int sms = 0;
+    if ((v = device_l2_bytes(&l2)) != STREAMKL_OK || (v = device_sms(&sms)) != STREAMKL_OK) return v;
+    bwd_mode = resolve_mutual_mode(p, bwd_mode, l2, sms);
+    range_tiles = fused_range_tiles(p, l2, sms);
+  }
+  if (bwd_mode == STREAMKL_BWD_FUSED) {
+    if (!workspace || !aligned16(workspace)) return STREAMKL_ERR_WORKSPACE;
+    if (workspace_bytes < fused_workspace_bytes(p, range_tiles)) return STREAMKL_ERR_WORKSPACE;
+  }
+  int* status = nullptr;
+  if ((v = status_ptr(&status)) != STREAMKL_OK) return v;
+  BwdIn in{q1, k1, q2, k2, lse1, lse2, kl, g};
+  if (bwd_mode == STREAMKL_BWD_SEPARATE) return from_cuda(launch_bwd_mutual(p, in, dq1, dk1, dq2, dk2, status, st));
+  // one fused pass per setting, one after the other on the stream, sharing the workspace
+  float* ws = static_cast<float*>(workspace);
+  cudaError_t e = launch_bwd_fused(p, 1, in, dq2, dk2, ws, range_tiles, status, st);
+  return from_cuda(e != cudaSuccess ? e : launch_bwd_fused(p, 2, in, dq1, dk1, ws, range_tiles, status, st));
 }
 
 streamkl_status streamkl_check_device_status(void* stream) {

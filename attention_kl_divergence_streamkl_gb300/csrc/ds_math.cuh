@@ -109,4 +109,36 @@ __device__ __forceinline__ void ds1_from_p1(const uint32_t (&s2)[N], const uint3
   }
 }
 
+// Both settings at once (the mutual case, where Q1/K1 and Q2/K2 all train):
+// dS1 = g P1 (r - KL) and dS2 = g (P2 - P1) from one read of the two logit
+// tiles, with the folded values nA, nB2 = -LSE2 log2(e) (setting 1's nB) and
+// nB1 = -(LSE1 - LSE2 + KL) (setting 2's nB).  The operations are ds_pair's of
+// each setting, so each output is bit-identical to that setting's dS.
+template <bool MASKED, int N>
+__device__ __forceinline__ void make_ds_row_mutual(const uint32_t* a, const uint32_t (&b)[N], uint32_t* pk1,
+                                                   uint32_t* pk2, float c, float scale, float nAr, float nB2r,
+                                                   float nB1r, float Gr, uint32_t visible) {
+  const float2 cc = make_float2(c, c), sc = make_float2(scale, scale);
+  const float2 nA = make_float2(nAr, nAr), nB2 = make_float2(nB2r, nB2r), nB1 = make_float2(nB1r, nB1r);
+  const float2 G = make_float2(Gr, Gr);
+#pragma unroll
+  for (int k = 0; k < N; k += 2) {
+    const float2 s1 = make_float2(__uint_as_float(a[k]), __uint_as_float(a[k + 1]));
+    const float2 s2 = make_float2(__uint_as_float(b[k]), __uint_as_float(b[k + 1]));
+    const float2 x1 = ffma2(s1, cc, nA), x2 = ffma2(s2, cc, nB2);
+    float2 p1 = make_float2(ex2(x1.x), ex2(x1.y)), p2 = make_float2(ex2(x2.x), ex2(x2.y));
+    if (MASKED) {
+      const bool k0 = (visible >> k) & 1u, k1 = (visible >> (k + 1)) & 1u;
+      p1.x = k0 ? p1.x : 0.f;
+      p1.y = k1 ? p1.y : 0.f;
+      p2.x = k0 ? p2.x : 0.f;
+      p2.y = k1 ? p2.y : 0.f;
+    }
+    const float2 d2 = fmul2(G, fsub2(p2, p1));
+    const float2 d1 = fmul2(fmul2(G, p1), ffma2(sc, fsub2(s1, s2), nB1));
+    pk1[k / 2] = pack_bf16(d1.x, d1.y);
+    pk2[k / 2] = pack_bf16(d2.x, d2.y);
+  }
+}
+
 }  // namespace skl

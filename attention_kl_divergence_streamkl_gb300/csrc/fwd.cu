@@ -54,6 +54,7 @@ constexpr float kFastSumLimit = 18446744073709551616.0f;  // 2^64
 constexpr uint32_t kTmemCols = 512;
 constexpr int kOneBlockPerSmSmem = 120 * 1024;
 constexpr long long kMaxPersistentRounds = 32;
+constexpr long long kMaxPersistentKeyTiles = 64;
 
 template <int D>
 struct Smem {
@@ -400,12 +401,15 @@ cudaError_t launch_d(const Problem& p, const void* q1, const void* k1, const voi
   e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
-  // Few rounds of items per SM: one block per SM walks them (the per-block set-up is paid once, and an item's
-  // closing step overlaps the next item's loads).  Many rounds: one block per item, so that the hardware's
-  // block scheduler balances the causal triangle and the blocks in flight stay on one head (a static walk
-  // measured 2% slower on B1 H32 N64K causal, and 6-8% faster on B2 H32 N4096).
+  // Short items in few rounds per SM: one block per SM walks them (the per-block set-up is paid once, and an
+  // item's closing step overlaps the next item's loads).  Otherwise one block per item, so that the hardware's
+  // block scheduler balances the causal triangle and the blocks in flight stay on one head.  Measured: the
+  // static walk is 6-8% faster on B2 H32 N4096 (32 key tiles, 13.5 rounds), 5% slower on B1 H4 N64K causal
+  // (512 key tiles, 13.5 rounds) and 2% slower on B1 H32 N64K causal (108 rounds).
   const long long rounds = (items + sms - 1) / sms;
-  const long long blocks = rounds <= kMaxPersistentRounds ? (items < sms ? items : sms) : items;
+  const long long key_tiles = (p.NK + BN - 1) / BN;
+  const bool walk = rounds <= kMaxPersistentRounds && key_tiles <= kMaxPersistentKeyTiles;
+  const long long blocks = walk ? (items < sms ? items : sms) : items;
   fwd_tc_kernel<D><<<(unsigned)blocks, THREADS, smem, st>>>(p, kl, lse1, lse2, part, status, mq1, mk1, mq2, mk2);
   return cudaGetLastError();
 }

@@ -77,6 +77,10 @@ cudaError_t launch_bwd_separate(const Problem& p, int setting, const BwdIn& in, 
 // workspace holds only the dK rows of one range.
 cudaError_t launch_bwd_fused(const Problem& p, int setting, const BwdIn& in, void* dq, void* dk, float* workspace,
                              int range_tiles, int* status, cudaStream_t st, float* dq_f32 = nullptr);
+// Both settings' gradients in one recompute (the mutual case): dQ1, dK1 (setting 2) and dQ2, dK2
+// (setting 1), each written with its input's strides; a dQ kernel, then a dK kernel, no workspace.
+cudaError_t launch_bwd_mutual(const Problem& p, const BwdIn& in, void* dq1, void* dk1, void* dq2, void* dk2,
+                              int* status, cudaStream_t st);
 // dK = 0 for every key row of every head, written with K's strides (a backward with no query rows).
 cudaError_t launch_zero_k_rows(const Problem& p, void* dk, cudaStream_t st);
 // out row n of head bh = bf16(scale * acc[bh][n]) for n < N_Q, with Q's strides.

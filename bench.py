@@ -54,13 +54,19 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="kl_b1h32_n65536_d128_causal")
     ap.add_argument("--setting", type=int, default=1, choices=[1, 2])
-    ap.add_argument("--bwd-mode", default="auto", choices=["auto", "fused", "separate"])
+    ap.add_argument("--bwd-mode", default="auto", choices=["auto", "fused", "separate", "mutual"],
+                    help="with --mutual: mutual = one recompute for both settings; fused / separate = a pass per "
+                         "setting")
     ap.add_argument("--nonsplit", action="store_true", help="decode workloads: time the non-split forward")
+    ap.add_argument("--mutual", action="store_true", help="both settings' gradients (Q1, K1, Q2, K2 all train)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--heads", type=int, default=0, help="override H (smaller cases for profiling)")
     ap.add_argument("--batch", type=int, default=0, help="override B (smaller cases for profiling)")
+    ap.add_argument("--nq", type=int, default=0, help="override N_Q")
+    ap.add_argument("--nk", type=int, default=0, help="override N_K")
+    ap.add_argument("--causal", type=int, default=-1, choices=[-1, 0, 1], help="override the mask (1 causal, 0 none)")
     ap.add_argument("--no-decode", action="store_true",
                     help="training workloads: skip the Split-K decode section of the JSON line")
     ap.add_argument("--decode-steps", type=int, default=10)
@@ -71,8 +77,12 @@ def parse():
 
 def pick_workload(synth, args):
     w = synth.WORKLOADS[args.workload]
-    if args.heads or args.batch:
-        w = w.with_(H=args.heads or w.H, B=args.batch or w.B, name=f"{w.name}[B={args.batch or w.B},H={args.heads or w.H}]")
+    over = {k: v for k, v in (("B", args.batch), ("H", args.heads), ("NQ", args.nq), ("NK", args.nk)) if v}
+    if args.causal >= 0:
+        over["causal"] = bool(args.causal)
+    if over:
+        tag = ",".join(f"{k}={int(v) if isinstance(v, bool) else v}" for k, v in over.items())
+        w = w.with_(name=f"{w.name}[{tag}]", **over)
     return w
 
 
@@ -245,7 +255,8 @@ def run_reference(args):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic",
             "config": {"workload": w.name, "B": w.B, "H": w.H, "N_Q": w.NQ, "N_K": w.NK, "D": w.D,
-                       "causal": w.causal, "setting": args.setting if not decode else None,
+                       "causal": w.causal,
+                       "setting": None if decode else ("mutual" if args.mutual else args.setting),
                        "path": ("oracle rows_forward" if decode else "oracle rows_forward + head_backward_rows"),
                        "per_gpu_units": "a bounded sample of the workload per step (see cpu_baseline.sample)",
                        "parallelism": "replicas1"},
@@ -333,8 +344,16 @@ def run_ours(args):
 
     w = pick_workload(synth, args)
     decode = w.name.startswith("decode")
-    mode = {"auto": skl.BWD_AUTO, "fused": skl.BWD_FUSED, "separate": skl.BWD_SEPARATE}[args.bwd_mode]
-    if not decode and mode == skl.BWD_AUTO:
+    mode = {"auto": skl.BWD_AUTO, "fused": skl.BWD_FUSED, "separate": skl.BWD_SEPARATE,
+            "mutual": "mutual"}[args.bwd_mode]
+    if mode == "mutual" and not args.mutual:
+        raise SystemExit("--bwd-mode mutual needs --mutual")
+    if args.mutual and not decode and mode == skl.BWD_AUTO:
+        props = torch.cuda.get_device_properties(dev)
+        pick = skl.bwd_mutual_select(w.B, w.H, w.NQ, w.NK, w.D, props.L2_cache_size, props.multi_processor_count,
+                                     w.causal)
+        mode = "mutual" if pick == skl.BWD_SEPARATE else skl.BWD_FUSED
+    elif not decode and mode == skl.BWD_AUTO:
         props = torch.cuda.get_device_properties(dev)
         mode = skl.bwd_select(w.B, w.H, w.NQ, w.NK, w.D, props.L2_cache_size, props.multi_processor_count,
                               w.causal)
@@ -369,6 +388,19 @@ def run_ours(args):
         kl, l1, l2 = skl.fwd(a, b, c, d, scale, causal)
         if ev:
             ev[1].record(stream)
+        if args.mutual:
+            if mode == "mutual":
+                grads = skl.bwd_mutual(a, b, c, d, l1, l2, kl, g_, scale, causal, skl.BWD_SEPARATE)
+                if ev:
+                    ev[2].record(stream)
+            else:
+                grads = skl.bwd_s1(a, b, c, d, l1, l2, g_, scale, causal, mode)
+                if ev:
+                    ev[2].record(stream)
+                grads = grads + skl.bwd_s2(a, b, c, d, l1, l2, kl, g_, scale, causal, mode)
+            if ev:
+                ev[3].record(stream)
+            return (kl,) + tuple(grads)
         bwd = skl.bwd_s1 if args.setting == 1 else skl.bwd_s2
         extra = () if args.setting == 1 else (kl,)
         if mode == skl.BWD_SEPARATE:
@@ -389,6 +421,22 @@ def run_ours(args):
         kernels = ["fwd" if args.nonsplit else "splitk"]
         algo = {kernels[0]: 4 * w.D * pairs}
         launches_per_step = 1 if args.nonsplit else 2
+    elif mode == "mutual":
+        kernels = ["fwd", "bwd_mutual", "none"]
+        algo = {"fwd": 4 * w.D * pairs, "bwd_mutual": 16 * w.D * pairs}
+        launches_per_step = 3
+    elif args.mutual:
+        tag = "fused" if mode == skl.BWD_FUSED else "separate"
+        kernels = ["fwd", f"bwd_s1_{tag}", f"bwd_s2_{tag}"]
+        algo = {"fwd": 4 * w.D * pairs, kernels[1]: 8 * w.D * pairs, kernels[2]: 8 * w.D * pairs}
+        props = torch.cuda.get_device_properties(dev)
+        key_ranges = skl.bwd_fused_plan(w.B, w.H, w.NQ, w.NK, w.D, props.L2_cache_size,
+                                        props.multi_processor_count, w.causal)[0]
+        if mode == skl.BWD_FUSED:
+            launches_per_step = 1 + 2 * (2 * key_ranges + (1 if key_ranges > 1 else 0))
+        else:
+            key_ranges = None
+            launches_per_step = 5
     elif mode == skl.BWD_SEPARATE:
         kernels = ["fwd", "bwd_dq", "bwd_dk"]
         algo = {"fwd": 4 * w.D * pairs, "bwd_dq": 6 * w.D * pairs, "bwd_dk": 6 * w.D * pairs}
@@ -449,9 +497,11 @@ def run_ours(args):
                 "traffic": NCU_TRAFFIC_RATIO[dom] * bytes_step if dom in NCU_TRAFFIC_RATIO else None,
                 "peak_source": f"{peak_src} hbm_gbs", "algorithmic_bytes_per_launch": bytes_step}
     else:
-        flops_step = 12 * w.D * pairs
+        flops_step = (20 if args.mutual else 12) * w.D * pairs
         value = whole_job_rate(flops_step, ms_step, world, 1e12)
         metric, unit = "attn-KL fwd+bwd TFLOP/s & ms (H32 D128 N64K causal), % bf16 TC peak", "TFLOP/s"
+        if args.mutual:
+            metric = "attn-KL fwd + both settings' bwd TFLOP/s (mutual case; 20D FLOP per unmasked pair)"
         dom = max(per_kernel, key=per_kernel.get)
         avg_ms = per_kernel[dom] / args.steps
         achieved = algo[dom] / (avg_ms / 1e3) / 1e12
@@ -511,7 +561,7 @@ def run_ours(args):
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu:
+    if rank == 0 and world == 1 and not args.no_cpu and not args.mutual:
         if decode:
             cpu = None
         else:
@@ -520,8 +570,8 @@ def run_ours(args):
                    "seconds": dt}
 
     decode_section = None
-    if not decode and not args.no_decode and args.workload == "kl_b1h32_n65536_d128_causal" and not (
-            args.heads or args.batch):
+    if not decode and not args.no_decode and not args.mutual and args.workload == "kl_b1h32_n65536_d128_causal" and not (
+            args.heads or args.batch or args.nq or args.nk or args.causal >= 0):
         del q1, k1, q2, k2
         torch.cuda.empty_cache()
         decode_section = time_decode(args, dev, peaks, peak_src)
@@ -531,7 +581,8 @@ def run_ours(args):
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": w.name, "B": w.B, "H": w.H, "N_Q": w.NQ, "N_K": w.NK, "D": w.D,
                        "causal": w.causal, "setting": args.setting if not decode else None,
-                       "layout": args.layout, "bwd_path": None if decode else {1: "fused", 2: "separate"}[mode],
+                       "layout": args.layout,
+                       "bwd_path": None if decode else {1: "fused", 2: "separate", "mutual": "mutual"}[mode],
                        "bwd_key_ranges": key_ranges,
                        "path": ("nonsplit" if args.nonsplit else "splitk") if decode else "fwd+bwd",
                        "per_gpu_units": "the whole workload on every rank (independent heads)",

@@ -255,6 +255,47 @@ streamkl_status streamkl_bwd_s2(const void* q1, const void* k1, const void* q2, 
                                 const float* kl, const float* g, void* dq1, void* dk1, int bwd_mode,
                                 void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * The mutual case: Q1, K1, Q2, K2 all optimised (both distributions train).
+ * (technical summary, 手法 2 "recompute strategy", settings 1 and 2.)
+ * P2 does not depend on Q1/K1 nor P1 on Q2/K2, so the gradients of
+ * L = sum_i g_i KL_i are setting 2's (dQ1, dK1) and setting 1's (dQ2, dK2).
+ * bwd_mode:
+ *   STREAMKL_BWD_SEPARATE  the mutual kernels: S1 and S2 of each tile pair are
+ *                          rebuilt once and both dS tiles formed from them (a
+ *                          dQ kernel, then a dK kernel, no atomics, no
+ *                          workspace); dS1 and dS2 are bit-identical to the
+ *                          single settings', and so are the four outputs to
+ *                          those of streamkl_bwd_s2 / streamkl_bwd_s1 with
+ *                          STREAMKL_BWD_SEPARATE.
+ *   STREAMKL_BWD_FUSED     one fused pass per setting (setting 1, then setting
+ *                          2), sharing the workspace of streamkl_bwd_workspace.
+ *   STREAMKL_BWD_AUTO      as streamkl_bwd_mutual_select decides.
+ * Arguments are those of streamkl_bwd_s2 (kl is required) with four bf16
+ * outputs, each [B,H,N,D] with the strides of its input (dq1: q1's strides,
+ * dk2: k2's, ...), all four non-NULL and 16-byte aligned.  Work runs on
+ * `stream`.  With N_Q = 0 both dK are written as zeros.  Errors:
+ * STREAMKL_ERR_INVALID for a bad shape, pointer or mode (DQ_ONLY / DK_ONLY are
+ * refused), STREAMKL_ERR_WORKSPACE when the fused passes are chosen and the
+ * workspace is missing or smaller than streamkl_bwd_mutual_workspace's,
+ * STREAMKL_ERR_UNSUPPORTED for D not in {64, 128}; nothing is launched then.
+ */
+streamkl_status streamkl_bwd_mutual(const void* q1, const void* k1, const void* q2, const void* k2,
+                                    streamkl_shape s, const float* lse1, const float* lse2,
+                                    const float* kl, const float* g, void* dq1, void* dk1,
+                                    void* dq2, void* dk2, int bwd_mode, void* workspace,
+                                    size_t workspace_bytes, void* stream);
+/*
+ * AUTO's choice for the mutual case on a device with `l2_bytes` of L2 and
+ * `num_sms` SMs (pure host rule): STREAMKL_BWD_SEPARATE (the mutual kernels)
+ * when the fused path would need more than one key range and a head has at
+ * most 16 query tiles of 128 rows, else STREAMKL_BWD_FUSED (a fused pass per
+ * setting), measured on GB300.  0 for an invalid shape.
+ */
+int streamkl_bwd_mutual_select(streamkl_shape s, size_t l2_bytes, int num_sms);
+/* Workspace bytes streamkl_bwd_mutual needs in `bwd_mode` on the current device (0 for the mutual kernels). */
+streamkl_status streamkl_bwd_mutual_workspace(streamkl_shape s, int bwd_mode, size_t* bytes);
+
 /* Text for a status code (static storage). */
 const char* streamkl_status_string(streamkl_status st);
 

@@ -285,3 +285,43 @@ def test_key_shard_entry_points_validate_before_any_launch(lib):
     # dQ from the summed partials: aligned buffers
     assert lib.streamkl_dq_from_partial(fake_ptr(4), sm, p[9], None) == K.ERR_INVALID
     assert lib.streamkl_dq_from_partial(p[8], sm, fake_ptr(2), None) == K.ERR_INVALID
+
+
+def test_bwd_mutual_select(lib):
+    """The mutual case: the mutual kernels where the fused path needs several key ranges and a head has at
+    most 16 query tiles; a fused pass per setting otherwise."""
+    l2, sms = 135528448, 152  # GB300
+    S = lambda *a: K.bwd_mutual_select(*a, l2, sms)  # noqa: E731
+    assert S(1, 32, 128, 65536, 128) == K.BWD_SEPARATE
+    assert S(1, 8, 1024, 65536, 128) == K.BWD_SEPARATE  # 8 query tiles, 5 key ranges
+    assert S(1, 8, 2048, 262144, 128) == K.BWD_SEPARATE  # 16 query tiles
+    assert S(1, 8, 2049, 262144, 128) == K.BWD_FUSED  # 17 query tiles
+    assert S(1, 32, 65536, 65536, 128) == K.BWD_FUSED  # one key range
+    assert S(2, 32, 4096, 4096, 128) == K.BWD_FUSED
+    assert S(1, 8, 524288, 524288, 128) == K.BWD_FUSED  # many query tiles
+    assert K.bwd_fused_plan(1, 8, 1024, 65536, 128, l2, sms, False)[0] > 1
+    assert K.bwd_mutual_select(0, 1, 8, 8, 64, l2, sms) == 0
+    assert K.bwd_mutual_select(1, 1, 8, 8, 64, l2, 0) == 0
+
+
+def test_bwd_mutual_validates_before_any_launch(lib):
+    s = K.make_shape(1, 1, 8, 8, 64)
+    p = [fake_ptr(64 * i) for i in range(16)]
+    ins, rows = p[:4], p[4:8]
+    outs = p[8:12]
+    n = ctypes.c_size_t(1)
+    for mode in (K.BWD_DQ_ONLY, K.BWD_DK_ONLY, 9):
+        assert lib.streamkl_bwd_mutual(*ins, s, *rows, *outs, mode, p[12], 1 << 20, None) == K.ERR_INVALID
+        assert lib.streamkl_bwd_mutual_workspace(s, mode, ctypes.byref(n)) == K.ERR_INVALID
+    assert lib.streamkl_bwd_mutual_workspace(s, K.BWD_SEPARATE, ctypes.byref(n)) == K.OK and n.value == 0
+    for k in range(4):  # every output is required and 16-byte aligned
+        bad = list(outs)
+        bad[k] = None
+        assert lib.streamkl_bwd_mutual(*ins, s, *rows, *bad, K.BWD_SEPARATE, None, 0, None) == K.ERR_INVALID
+        bad[k] = fake_ptr(2)
+        assert lib.streamkl_bwd_mutual(*ins, s, *rows, *bad, K.BWD_SEPARATE, None, 0, None) == K.ERR_INVALID
+    assert lib.streamkl_bwd_mutual(*ins, s, rows[0], rows[1], None, rows[3], *outs, K.BWD_SEPARATE, None, 0,
+                                   None) == K.ERR_INVALID  # the saved KL is required
+    assert lib.streamkl_bwd_mutual(*ins, s, *rows, *outs, K.BWD_FUSED, None, 0, None) == K.ERR_WORKSPACE
+    assert lib.streamkl_bwd_mutual(*ins, s, *rows, *outs, K.BWD_FUSED, fake_ptr(8), 1 << 20,
+                                   None) == K.ERR_WORKSPACE  # misaligned workspace
