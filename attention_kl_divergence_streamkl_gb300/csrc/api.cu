@@ -171,39 +171,43 @@ size_t fused_workspace_bytes(const Problem& p, int range_tiles) {
 }
 
 // AUTO takes the fused path (over key ranges it keeps its atomics in L2 for any
-// N_K) unless a head has at most two query tiles and the fused path needs more
-// than one key range: each key tile is then reused by at most two query tiles,
-// so the fused kernel's one visit per tile pair saves little, while its dK
-// atomics and per-range dQ round trips cost more than the separate kernels'
-// recompute (measured: B1 H128 N_Q=128 N_K=64K 3.46 ms separate vs 4.24 fused,
-// B1 H64 N_Q=256 N_K=128K 4.73 vs 5.05; with 4 query tiles, B1 H32 N_Q=512
-// N_K=256K, the fused path wins, 7.19 vs 7.51).  Every other mode stands as given.
+// N_K) unless a head has at most kSeparateMaxQTiles query tiles and the fused
+// path would either need more than one key range or leave SMs idle (fewer
+// fused blocks, one per query tile, than SMs).  A key tile is then reused by
+// few query tiles, so the fused kernel's one visit per tile pair saves little,
+// while its dK atomics and per-range dQ round trips cost more than the separate
+// kernels' second recompute -- and the separate path's dK grid, many short
+// blocks, fills the SMs that its few long dQ blocks leave free, both grids in
+// one launch (the "separate kernels under contention" rule of the technical
+// summary, section 手法 2 "kernel fusion").
+// Measured on B1 H8 N_K=64K non-causal, ms for setting 1's backward, separate
+// against fused: N_Q=512 0.71 / 1.24, N_Q=1024 0.76 / 1.24, N_Q=2048 1.39 /
+// 1.25, N_Q=4096 2.64 / 2.33; B1 H32 N_Q=128 N_K=64K 0.84 / 1.74.
+constexpr int kSeparateMaxQTiles = 8;
 int resolve_bwd_mode(const Problem& p, int mode, size_t l2_bytes, int num_sms) {
   if (mode != STREAMKL_BWD_AUTO) return mode;
   const int n_qt = (p.NQ + 127) / 128, n_kt = (p.NK + 127) / 128;
-  if (n_qt <= 2 && fused_range_tiles(p, l2_bytes, num_sms) < n_kt) return STREAMKL_BWD_SEPARATE;
+  const bool idle_sms = (long long)p.BH * n_qt < num_sms;
+  if (n_qt <= kSeparateMaxQTiles && (idle_sms || fused_range_tiles(p, l2_bytes, num_sms) < n_kt))
+    return STREAMKL_BWD_SEPARATE;
   return STREAMKL_BWD_FUSED;
 }
 
 // The mutual case (both settings' gradients): AUTO takes the mutual kernels
 // (one recompute of each logit tile pair for both settings, reported as
-// STREAMKL_BWD_SEPARATE) when the fused path would run over several key ranges
-// and a head has at most kMutualMaxQTiles query tiles; there every key tile is
-// reused by few query tiles, and the fused path's dK atomics and per-range dQ
-// round trips, paid twice, outweigh the mutual kernels' second recompute
-// (measured, ms for both settings' backward, non-causal N_K = 64K: B1 H32
-// N_Q=128 2.07 mutual, 3.52 two fused passes, 2.84 two separate passes; B1 H8
-// N_Q=1024 1.84, 2.50, 2.43; N_Q=2048 2.36, 2.54, 3.13; N_Q=4096 4.54, 4.71,
-// 5.96 -- the gain shrinks as query tiles grow).  Otherwise one fused pass per
-// setting, which wins when the fused path keeps all keys in one range (B1 H8
-// N64K causal 32.3 mutual against 30.3; B1 H8 N16K causal 2.23 against 2.10;
-// B2 H32 N4096 non-causal 2.28 against 2.18, causal 1.29 against 1.30).
-constexpr int kMutualMaxQTiles = 16;
+// STREAMKL_BWD_SEPARATE) when a head has at most kMutualMaxQTiles query tiles,
+// else one fused pass per setting.  Measured, ms for both settings' backward
+// (mutual against two fused passes): B1 H32 N_Q=128 N_K=64K non-causal 1.16 /
+// 3.52; B1 H8 N_K=64K non-causal N_Q=1024 1.16 / 2.50, N_Q=4096 4.13 / 4.69,
+// N_Q=8192 8.11 / 8.82; causal B2 H32 N4096 1.23 / 1.30, B1 H8 N8K 0.62 / 0.68,
+// N16K 2.15 / 2.10, N32K 8.10 / 7.65, N64K 31.9 / 30.3; B1 H4 N64K non-causal
+// 31.9 / 30.6; B1 H2 N512K causal 508 / 492.
+constexpr int kMutualMaxQTiles = 64;
 int resolve_mutual_mode(const Problem& p, int mode, size_t l2_bytes, int num_sms) {
+  (void)l2_bytes;
+  (void)num_sms;
   if (mode != STREAMKL_BWD_AUTO) return mode;
-  const int n_qt = (p.NQ + 127) / 128, n_kt = (p.NK + 127) / 128;
-  if (n_qt <= kMutualMaxQTiles && fused_range_tiles(p, l2_bytes, num_sms) < n_kt) return STREAMKL_BWD_SEPARATE;
-  return STREAMKL_BWD_FUSED;
+  return (p.NQ + 127) / 128 <= kMutualMaxQTiles ? STREAMKL_BWD_SEPARATE : STREAMKL_BWD_FUSED;
 }
 
 streamkl_status device_l2_bytes(size_t* out) {

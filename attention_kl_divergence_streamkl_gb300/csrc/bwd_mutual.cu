@@ -6,13 +6,14 @@
 // "recompute strategy" and its two settings.  Neither setting's gradient
 // depends on the other side's parameters, so the mutual gradient is the pair
 // of single-setting gradients; what the two settings share is the recompute:
-// both need S1 and S2 of every tile pair.  These kernels read the two logit
+// both need S1 and S2 of every tile pair.  These blocks read the two logit
 // tiles once and produce both dS tiles from them (make_ds_row_mutual), where
 // running the settings one after the other computes every logit tile twice.
 //
-// Two kernels, like the separate single-setting path (no atomics):
+// Two kinds of block, like the separate single-setting path's two kernels (no
+// atomics), run as one launch (bwd_mutual_kernel):
 //
-// dQ kernel: a block owns 128 query rows (Q1, Q2 stationary) and streams key tiles:
+// dQ blocks: a block owns 128 query rows (Q1, Q2 stationary) and streams key tiles:
 //     S1 = Q1 K1^T, then S2 = Q2 K2^T     both into TMEM columns [0, 128)
 //     dS1, dS2 packed to bf16 into TMEM   [128, 192), [192, 256)
 //     dQ1 += dS1 K1, dQ2 += dS2 K2        A = dS in TMEM, B = K read MN-major -> [256, 256 + D), [384, 384 + D)
@@ -24,7 +25,7 @@
 //               takes key columns [32g, 32g + 32); at the end they write dQ1 and dQ2
 //   warp 16     TMA producer        warp 17  TMEM owner and MMA issuer
 //
-// dK kernel: a block owns 128 keys (K1, K2 stationary) and streams query tiles as
+// dK blocks: a block owns 128 keys (K1, K2 stationary) and streams query tiles as
 // the M operand of the logits MMA, so a dS thread owns a query row:
 //     S1 = Q1 K1^T -> [0, 128), S2 = Q2 K2^T -> [128, 256)
 //     dS1, then dS2, to one shared-memory buffer as dS[query][key]
@@ -82,7 +83,7 @@ __device__ __forceinline__ RowVals row_vals(const float* lse1, const float* lse2
   return RowVals{-l1v * kLog2e, -l2v * kLog2e, -(l1v - l2v + klv[o]), gv[o]};
 }
 
-// ============================================================================ dQ kernel
+// ============================================================================ dQ blocks
 namespace mdq {
 constexpr int BX = 128, BY = 128, SLOTS = 5;
 constexpr uint32_t kColS = 0, kColDS1 = 128, kColDS2 = 192, kColG1 = 256, kColG2 = 384;
@@ -102,13 +103,14 @@ struct Smem {
 static_assert(Smem<128>::BYTES <= 227 * 1024, "shared memory");
 }  // namespace mdq
 
+// Block `blk` of the dQ grid (head-major, the last query tiles first).
 template <int D>
-__global__ void __launch_bounds__(THREADS, 1)
-    bwd_dq_mutual_kernel(const Problem p, const float* __restrict__ lse1, const float* __restrict__ lse2,
-                         const float* __restrict__ klv, const float* __restrict__ gv, __nv_bfloat16* __restrict__ dq1,
-                         __nv_bfloat16* __restrict__ dq2, int* status, const __grid_constant__ CUtensorMap mq1,
-                         const __grid_constant__ CUtensorMap mq2, const __grid_constant__ CUtensorMap mk1,
-                         const __grid_constant__ CUtensorMap mk2) {
+__device__ __forceinline__ void dq_mutual_block(const Problem& p, const float* __restrict__ lse1,
+                                                const float* __restrict__ lse2, const float* __restrict__ klv,
+                                                const float* __restrict__ gv, __nv_bfloat16* __restrict__ dq1,
+                                                __nv_bfloat16* __restrict__ dq2, int* status, const CUtensorMap& mq1,
+                                                const CUtensorMap& mq2, const CUtensorMap& mk1, const CUtensorMap& mk2,
+                                                const unsigned blk) {
   using namespace mdq;
   using L = Smem<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -117,9 +119,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_xt = (p.NQ + BX - 1) / BX;
   // heads in order, the last query tiles (the most keys when causal) first within a head
-  const int bh = (int)(blockIdx.x / n_xt);
+  const int bh = (int)(blk / n_xt);
   const int mh = bh % p.H, mb = bh / p.H;
-  const int xt = n_xt - 1 - (int)(blockIdx.x % n_xt);
+  const int xt = n_xt - 1 - (int)(blk % n_xt);
   const int x0 = xt * BX;
   const int y_end = p.causal ? min(p.NK, min(p.NQ, x0 + BX) - 1 + p.off + 1) : p.NK;  // keys the last row sees
   const int n_yt = (y_end + BY - 1) / BY;
@@ -327,7 +329,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
-// ============================================================================ dK kernel
+// ============================================================================ dK blocks
 namespace mdk {
 constexpr int BK = 128, BQ = 128, SLOTS = 4;
 constexpr uint32_t kColSA = 0, kColSB = 128, kColG1 = 256, kColG2 = 384;
@@ -348,13 +350,14 @@ struct Smem {
 static_assert(Smem<128>::BYTES <= 227 * 1024, "shared memory");
 }  // namespace mdk
 
+// Block `blk` of the dK grid (head-major, the first key tiles first).
 template <int D>
-__global__ void __launch_bounds__(THREADS, 1)
-    bwd_dk_mutual_kernel(const Problem p, const float* __restrict__ lse1, const float* __restrict__ lse2,
-                         const float* __restrict__ klv, const float* __restrict__ gv, __nv_bfloat16* __restrict__ dk1,
-                         __nv_bfloat16* __restrict__ dk2, int* status, const __grid_constant__ CUtensorMap mk1,
-                         const __grid_constant__ CUtensorMap mk2, const __grid_constant__ CUtensorMap mq1,
-                         const __grid_constant__ CUtensorMap mq2) {
+__device__ __forceinline__ void dk_mutual_block(const Problem& p, const float* __restrict__ lse1,
+                                                const float* __restrict__ lse2, const float* __restrict__ klv,
+                                                const float* __restrict__ gv, __nv_bfloat16* __restrict__ dk1,
+                                                __nv_bfloat16* __restrict__ dk2, int* status, const CUtensorMap& mk1,
+                                                const CUtensorMap& mk2, const CUtensorMap& mq1, const CUtensorMap& mq2,
+                                                const unsigned blk) {
   using namespace mdk;
   using L = Smem<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -363,9 +366,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // heads in order; within a head the first key tiles (seen by the most queries when causal) first
   const int n_kt_all = (p.NK + BK - 1) / BK;
-  const int bh = (int)(blockIdx.x / n_kt_all);
+  const int bh = (int)(blk / n_kt_all);
   const int mh = bh % p.H, mb = bh / p.H;
-  const int k0 = (int)(blockIdx.x % n_kt_all) * BK;
+  const int k0 = (int)(blk % n_kt_all) * BK;
   const int q_begin = p.causal ? max(0, k0 - p.off) / BQ * BQ : 0;
   const int n_qt = (p.NQ - q_begin + BQ - 1) / BQ;
   const int n_items = 2 * n_qt;  // ring items: Q1(j) = 2j, Q2(j) = 2j + 1
@@ -598,6 +601,26 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
+// Both grids in one launch: blocks [0, n_first) are the first kind's, the rest the other's (dq_first picks
+// which comes first: the kind whose blocks walk more tiles).  The grids share no data; with few query tiles
+// the dQ grid has few, long blocks and the dK grid many short ones that fill the SMs the former leave idle.
+template <int D>
+__global__ void __launch_bounds__(THREADS, 1)
+    bwd_mutual_kernel(const Problem p, const float* __restrict__ lse1, const float* __restrict__ lse2,
+                      const float* __restrict__ klv, const float* __restrict__ gv, __nv_bfloat16* __restrict__ dq1,
+                      __nv_bfloat16* __restrict__ dk1, __nv_bfloat16* __restrict__ dq2,
+                      __nv_bfloat16* __restrict__ dk2, int* status, const __grid_constant__ CUtensorMap mq1,
+                      const __grid_constant__ CUtensorMap mq2, const __grid_constant__ CUtensorMap mk1,
+                      const __grid_constant__ CUtensorMap mk2, const unsigned n_first, const int dq_first) {
+  const unsigned b = blockIdx.x;
+  const bool is_dq = dq_first ? b < n_first : b >= n_first;
+  const unsigned blk = b < n_first ? b : b - n_first;
+  if (is_dq)
+    dq_mutual_block<D>(p, lse1, lse2, klv, gv, dq1, dq2, status, mq1, mq2, mk1, mk2, blk);
+  else
+    dk_mutual_block<D>(p, lse1, lse2, klv, gv, dk1, dk2, status, mk1, mk2, mq1, mq2, blk);
+}
+
 template <int D>
 cudaError_t mutual_d(const Problem& p, const BwdIn& in, void* dq1, void* dk1, void* dq2, void* dk2, int* status,
                      cudaStream_t st) {
@@ -605,25 +628,19 @@ cudaError_t mutual_d(const Problem& p, const BwdIn& in, void* dq1, void* dk1, vo
   if (!encode_q_map(&mq1, in.q1, p, 128) || !encode_q_map(&mq2, in.q2, p, 128) ||
       !encode_k_map(&mk1, in.k1, p, 128) || !encode_k_map(&mk2, in.k2, p, 128))
     return cudaErrorInvalidValue;
-  {
-    const int smem = mdq::Smem<D>::BYTES > kOneBlockPerSmSmem ? mdq::Smem<D>::BYTES : kOneBlockPerSmSmem;
-    auto kern = bwd_dq_mutual_kernel<D>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    const long long blocks = (long long)p.BH * ((p.NQ + mdq::BX - 1) / mdq::BX);
-    kern<<<(unsigned)blocks, THREADS, smem, st>>>(p, in.lse1, in.lse2, in.kl, in.g,
-                                                  static_cast<__nv_bfloat16*>(dq1), static_cast<__nv_bfloat16*>(dq2),
-                                                  status, mq1, mq2, mk1, mk2);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-  }
-  const int smem = mdk::Smem<D>::BYTES > kOneBlockPerSmSmem ? mdk::Smem<D>::BYTES : kOneBlockPerSmSmem;
-  auto kern = bwd_dk_mutual_kernel<D>;
+  int smem = kOneBlockPerSmSmem;
+  if (mdq::Smem<D>::BYTES > smem) smem = mdq::Smem<D>::BYTES;
+  if (mdk::Smem<D>::BYTES > smem) smem = mdk::Smem<D>::BYTES;
+  auto kern = bwd_mutual_kernel<D>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  const long long blocks = (long long)p.BH * ((p.NK + mdk::BK - 1) / mdk::BK);
-  kern<<<(unsigned)blocks, THREADS, smem, st>>>(p, in.lse1, in.lse2, in.kl, in.g, static_cast<__nv_bfloat16*>(dk1),
-                                                static_cast<__nv_bfloat16*>(dk2), status, mk1, mk2, mq1, mq2);
+  const long long dq_blocks = (long long)p.BH * ((p.NQ + mdq::BX - 1) / mdq::BX);
+  const long long dk_blocks = (long long)p.BH * ((p.NK + mdk::BK - 1) / mdk::BK);
+  const int dq_first = p.NK >= p.NQ;  // a dQ block walks the keys, a dK block the queries
+  kern<<<(unsigned)(dq_blocks + dk_blocks), THREADS, smem, st>>>(
+      p, in.lse1, in.lse2, in.kl, in.g, static_cast<__nv_bfloat16*>(dq1), static_cast<__nv_bfloat16*>(dk1),
+      static_cast<__nv_bfloat16*>(dq2), static_cast<__nv_bfloat16*>(dk2), status, mq1, mq2, mk1, mk2,
+      (unsigned)(dq_first ? dq_blocks : dk_blocks), dq_first);
   return cudaGetLastError();
 }
 

@@ -10,8 +10,8 @@
 // In both kernels the 128 TMEM lanes of the logits are queries, so a dS thread
 // owns a query row and holds its folded LSE1, LSE2, g, KL in registers.
 //
-// dQ kernel: a block owns 128 query rows X (Q1, Q2 stationary) and streams key
-// tiles Y:
+// dQ kernel (dq_block): a block owns 128 query rows X (Q1, Q2 stationary) and
+// streams key tiles Y:
 //     S1 = X1 Y1^T, S2 = X2 Y2^T          (tcgen05, both operands K-major in smem)
 //     dS from S1, S2 and the row's values, packed to bf16 into TMEM
 //     G += dS Y_opt                       (tcgen05, A = dS in TMEM, B = Y_opt
@@ -28,8 +28,12 @@
 //   warp 17     TMEM owner and MMA issuer; issues S(j) before G += dS(j-1)
 // Warpgroup 4 gives registers to the dS warpgroups (setmaxnreg).
 //
-// The dK kernel (bwd_dk_kernel, below) keeps 128 keys stationary and streams
-// query tiles as the M operand of the logits MMA; see its own comment.
+// The dK kernel (dk_block, below) keeps 128 keys stationary and streams
+// query tiles as the M operand of the logits MMA; see its own comment.  When
+// both gradients are wanted the two grids run as one launch (bwd_dqdk_kernel).
+// A dQ block walks the key tiles and a dK block the query tiles, so with few
+// query tiles the dQ grid has few, long blocks and the dK grid many short ones:
+// in one launch the dK blocks fill the SMs the dQ blocks leave idle.
 #include "common.cuh"
 #include "ds_math.cuh"
 #include "kernels.h"
@@ -72,12 +76,13 @@ __device__ __forceinline__ void setmaxnreg_dec_other() {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsOther));
 }
 
+// One block of the dQ kernel: block `blk` of the dQ grid (head-major, the last query tiles first).
 template <int D, int SETTING>
-__global__ void __launch_bounds__(THREADS, 1)
-    bwd_dq_kernel(const Problem p, const float* __restrict__ lse1, const float* __restrict__ lse2,
-                  const float* __restrict__ klv, const float* __restrict__ gv, __nv_bfloat16* __restrict__ out,
-                  int* status, const __grid_constant__ CUtensorMap mx1, const __grid_constant__ CUtensorMap mx2,
-                  const __grid_constant__ CUtensorMap my1, const __grid_constant__ CUtensorMap my2) {
+__device__ __forceinline__ void dq_block(const Problem& p, const float* __restrict__ lse1,
+                                         const float* __restrict__ lse2, const float* __restrict__ klv,
+                                         const float* __restrict__ gv, __nv_bfloat16* __restrict__ out, int* status,
+                                         const CUtensorMap& mx1, const CUtensorMap& mx2, const CUtensorMap& my1,
+                                         const CUtensorMap& my2, const unsigned blk) {
   using L = Smem<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
@@ -87,9 +92,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int n_xt = (NX + BX - 1) / BX;
   // heads in order (the blocks in flight share one head's K tiles in L2), longest blocks (the last query
   // tiles) first within a head
-  const int bh = (int)(blockIdx.x / n_xt);
+  const int bh = (int)(blk / n_xt);
   const int mh = bh % p.H, mb = bh / p.H;  // head and batch coordinates of the tensor maps
-  const int xt = n_xt - 1 - (int)(blockIdx.x % n_xt);
+  const int xt = n_xt - 1 - (int)(blk % n_xt);
   const int x0 = xt * BX;
   const int y_end = p.causal ? min(NY, min(NX, x0 + BX) - 1 + p.off + 1) : NY;  // keys the last row sees
   const int n_yt = (y_end + BY - 1) / BY;
@@ -349,12 +354,13 @@ struct Smem {
 static_assert(Smem<128>::BYTES <= 227 * 1024, "shared memory");
 }  // namespace dkk
 
+// One block of the dK kernel: block `blk` of the dK grid (head-major, the first key tiles first).
 template <int D, int SETTING>
-__global__ void __launch_bounds__(THREADS, 1)
-    bwd_dk_kernel(const Problem p, const float* __restrict__ lse1, const float* __restrict__ lse2,
-                  const float* __restrict__ klv, const float* __restrict__ gv, __nv_bfloat16* __restrict__ dk_out,
-                  int* status, const __grid_constant__ CUtensorMap mk1, const __grid_constant__ CUtensorMap mk2,
-                  const __grid_constant__ CUtensorMap mq1, const __grid_constant__ CUtensorMap mq2) {
+__device__ __forceinline__ void dk_block(const Problem& p, const float* __restrict__ lse1,
+                                         const float* __restrict__ lse2, const float* __restrict__ klv,
+                                         const float* __restrict__ gv, __nv_bfloat16* __restrict__ dk_out, int* status,
+                                         const CUtensorMap& mk1, const CUtensorMap& mk2, const CUtensorMap& mq1,
+                                         const CUtensorMap& mq2, const unsigned blk) {
   using dkk::BK;
   using dkk::BQ;
   using dkk::SLOTS;
@@ -366,9 +372,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   // heads in order (the blocks in flight share one head's Q tiles in L2); within a head the first key
   // tiles, which see the most queries, first
   const int n_kt_all = (p.NK + BK - 1) / BK;
-  const int bh = (int)(blockIdx.x / n_kt_all);
+  const int bh = (int)(blk / n_kt_all);
   const int mh = bh % p.H, mb = bh / p.H;  // head and batch coordinates of the tensor maps
-  const int kt = (int)(blockIdx.x % n_kt_all);
+  const int kt = (int)(blk % n_kt_all);
   const int k0 = kt * BK;
   const int q_begin = p.causal ? max(0, k0 - p.off) / BQ * BQ : 0;
   const int n_qt = (p.NQ - q_begin + BQ - 1) / BQ;
@@ -628,49 +634,87 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
-constexpr int kOneBlockPerSmSmem = 120 * 1024;  // a block owns all 512 TMEM columns
-
 template <int D, int SETTING>
-cudaError_t launch_dq(const Problem& p, const BwdIn& in, void* dq, int* status, cudaStream_t st) {
-  CUtensorMap mx1, mx2, my1, my2;
-  if (!encode_q_map(&mx1, in.q1, p, BX) || !encode_q_map(&mx2, in.q2, p, BX) ||
-      !encode_k_map(&my1, in.k1, p, BY) || !encode_k_map(&my2, in.k2, p, BY))
-    return cudaErrorInvalidValue;
-  const int smem = Smem<D>::BYTES > kOneBlockPerSmSmem ? Smem<D>::BYTES : kOneBlockPerSmSmem;
-  auto kern = bwd_dq_kernel<D, SETTING>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
-  const long long blocks = (long long)p.BH * ((p.NQ + BX - 1) / BX);
-  kern<<<(unsigned)blocks, THREADS, smem, st>>>(p, in.lse1, in.lse2, in.kl, in.g, static_cast<__nv_bfloat16*>(dq),
-                                                status, mx1, mx2, my1, my2);
-  return cudaGetLastError();
+__global__ void __launch_bounds__(THREADS, 1)
+    bwd_dq_kernel(const Problem p, const float* __restrict__ lse1, const float* __restrict__ lse2,
+                  const float* __restrict__ klv, const float* __restrict__ gv, __nv_bfloat16* __restrict__ out,
+                  int* status, const __grid_constant__ CUtensorMap mq1, const __grid_constant__ CUtensorMap mq2,
+                  const __grid_constant__ CUtensorMap mk1, const __grid_constant__ CUtensorMap mk2) {
+  dq_block<D, SETTING>(p, lse1, lse2, klv, gv, out, status, mq1, mq2, mk1, mk2, blockIdx.x);
 }
 
 template <int D, int SETTING>
-cudaError_t launch_dk(const Problem& p, const BwdIn& in, void* dk, int* status, cudaStream_t st) {
-  CUtensorMap mk1, mk2, mq1, mq2;
-  if (!encode_k_map(&mk1, in.k1, p, dkk::BK) || !encode_k_map(&mk2, in.k2, p, dkk::BK) ||
-      !encode_q_map(&mq1, in.q1, p, dkk::BQ) || !encode_q_map(&mq2, in.q2, p, dkk::BQ))
+__global__ void __launch_bounds__(THREADS, 1)
+    bwd_dk_kernel(const Problem p, const float* __restrict__ lse1, const float* __restrict__ lse2,
+                  const float* __restrict__ klv, const float* __restrict__ gv, __nv_bfloat16* __restrict__ dk_out,
+                  int* status, const __grid_constant__ CUtensorMap mq1, const __grid_constant__ CUtensorMap mq2,
+                  const __grid_constant__ CUtensorMap mk1, const __grid_constant__ CUtensorMap mk2) {
+  dk_block<D, SETTING>(p, lse1, lse2, klv, gv, dk_out, status, mk1, mk2, mq1, mq2, blockIdx.x);
+}
+
+// The dQ and the dK grids in one launch: blocks [0, n_first) are the first kind's, the rest the other's
+// (dq_first picks which comes first: the kind whose blocks walk more tiles).  The two kinds share no data, so
+// the short blocks of one fill the SMs the long blocks of the other leave free -- with few query tiles the dQ
+// grid alone has a block per head.
+template <int D, int SETTING>
+__global__ void __launch_bounds__(THREADS, 1)
+    bwd_dqdk_kernel(const Problem p, const float* __restrict__ lse1, const float* __restrict__ lse2,
+                    const float* __restrict__ klv, const float* __restrict__ gv, __nv_bfloat16* __restrict__ dq_out,
+                    __nv_bfloat16* __restrict__ dk_out, int* status, const __grid_constant__ CUtensorMap mq1,
+                    const __grid_constant__ CUtensorMap mq2, const __grid_constant__ CUtensorMap mk1,
+                    const __grid_constant__ CUtensorMap mk2, const unsigned n_first, const int dq_first) {
+  const unsigned b = blockIdx.x;
+  const bool is_dq = dq_first ? b < n_first : b >= n_first;
+  const unsigned blk = b < n_first ? b : b - n_first;
+  if (is_dq)
+    dq_block<D, SETTING>(p, lse1, lse2, klv, gv, dq_out, status, mq1, mq2, mk1, mk2, blk);
+  else
+    dk_block<D, SETTING>(p, lse1, lse2, klv, gv, dk_out, status, mk1, mk2, mq1, mq2, blk);
+}
+
+constexpr int kOneBlockPerSmSmem = 120 * 1024;  // a block owns all 512 TMEM columns
+
+template <int D, int SETTING>
+cudaError_t launch_sep(const Problem& p, const BwdIn& in, void* dq, void* dk, int* status, cudaStream_t st) {
+  static_assert(BX == 128 && BY == 128 && dkk::BK == 128 && dkk::BQ == 128, "one box height for every map");
+  CUtensorMap mq1, mq2, mk1, mk2;
+  if (!encode_q_map(&mq1, in.q1, p, 128) || !encode_q_map(&mq2, in.q2, p, 128) ||
+      !encode_k_map(&mk1, in.k1, p, 128) || !encode_k_map(&mk2, in.k2, p, 128))
     return cudaErrorInvalidValue;
-  const int smem = dkk::Smem<D>::BYTES > kOneBlockPerSmSmem ? dkk::Smem<D>::BYTES : kOneBlockPerSmSmem;
-  auto kern = bwd_dk_kernel<D, SETTING>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
-  const long long blocks = (long long)p.BH * ((p.NK + dkk::BK - 1) / dkk::BK);
-  kern<<<(unsigned)blocks, THREADS, smem, st>>>(p, in.lse1, in.lse2, in.kl, in.g, static_cast<__nv_bfloat16*>(dk),
-                                                status, mk1, mk2, mq1, mq2);
+  const long long dq_blocks = (long long)p.BH * ((p.NQ + BX - 1) / BX);
+  const long long dk_blocks = (long long)p.BH * ((p.NK + dkk::BK - 1) / dkk::BK);
+  auto* dq_out = static_cast<__nv_bfloat16*>(dq);
+  auto* dk_out = static_cast<__nv_bfloat16*>(dk);
+  int smem = kOneBlockPerSmSmem;
+  if (dq && Smem<D>::BYTES > smem) smem = Smem<D>::BYTES;
+  if (dk && dkk::Smem<D>::BYTES > smem) smem = dkk::Smem<D>::BYTES;
+  cudaError_t e;
+  if (dq && dk) {
+    auto kern = bwd_dqdk_kernel<D, SETTING>;
+    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess) return e;
+    const int dq_first = p.NK >= p.NQ;  // a dQ block walks the keys, a dK block the queries
+    kern<<<(unsigned)(dq_blocks + dk_blocks), THREADS, smem, st>>>(p, in.lse1, in.lse2, in.kl, in.g, dq_out, dk_out,
+                                                                   status, mq1, mq2, mk1, mk2,
+                                                                   (unsigned)(dq_first ? dq_blocks : dk_blocks),
+                                                                   dq_first);
+  } else if (dq) {
+    auto kern = bwd_dq_kernel<D, SETTING>;
+    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess) return e;
+    kern<<<(unsigned)dq_blocks, THREADS, smem, st>>>(p, in.lse1, in.lse2, in.kl, in.g, dq_out, status, mq1, mq2, mk1,
+                                                     mk2);
+  } else if (dk) {
+    auto kern = bwd_dk_kernel<D, SETTING>;
+    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess) return e;
+    kern<<<(unsigned)dk_blocks, THREADS, smem, st>>>(p, in.lse1, in.lse2, in.kl, in.g, dk_out, status, mq1, mq2, mk1,
+                                                     mk2);
+  }
   return cudaGetLastError();
 }
 
 template <int D>
 cudaError_t separate_d(const Problem& p, int setting, const BwdIn& in, void* dq, void* dk, int* status,
                        cudaStream_t st) {
-  if (dq) {
-    cudaError_t e = setting == 1 ? launch_dq<D, 1>(p, in, dq, status, st) : launch_dq<D, 2>(p, in, dq, status, st);
-    if (e != cudaSuccess) return e;
-  }
-  if (!dk) return cudaSuccess;
-  return setting == 1 ? launch_dk<D, 1>(p, in, dk, status, st) : launch_dk<D, 2>(p, in, dk, status, st);
+  return setting == 1 ? launch_sep<D, 1>(p, in, dq, dk, status, st) : launch_sep<D, 2>(p, in, dq, dk, status, st);
 }
 
 }  // namespace

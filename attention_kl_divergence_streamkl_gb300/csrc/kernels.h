@@ -65,7 +65,8 @@ struct BwdIn {
   const void *q1, *k1, *q2, *k2;
   const float *lse1, *lse2, *kl, *g;
 };
-// setting 1: dq/dk are dQ2/dK2; setting 2: dQ1/dK1.  The separate path skips a NULL output.
+// setting 1: dq/dk are dQ2/dK2; setting 2: dQ1/dK1.  The separate path skips a NULL output; with both
+// outputs its dQ and dK grids run as one launch.
 cudaError_t launch_bwd_separate(const Problem& p, int setting, const BwdIn& in, void* dq, void* dk, int* status,
                                 cudaStream_t st);
 // Fused backward over key ranges of range_tiles 128-key tiles (all keys when
@@ -78,7 +79,7 @@ cudaError_t launch_bwd_separate(const Problem& p, int setting, const BwdIn& in, 
 cudaError_t launch_bwd_fused(const Problem& p, int setting, const BwdIn& in, void* dq, void* dk, float* workspace,
                              int range_tiles, int* status, cudaStream_t st, float* dq_f32 = nullptr);
 // Both settings' gradients in one recompute (the mutual case): dQ1, dK1 (setting 2) and dQ2, dK2
-// (setting 1), each written with its input's strides; a dQ kernel, then a dK kernel, no workspace.
+// (setting 1), each written with its input's strides; the dQ and the dK blocks in one launch, no workspace.
 cudaError_t launch_bwd_mutual(const Problem& p, const BwdIn& in, void* dq1, void* dk1, void* dq2, void* dk2,
                               int* status, cudaStream_t st);
 // dK = 0 for every key row of every head, written with K's strides (a backward with no query rows).

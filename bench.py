@@ -32,7 +32,7 @@ import numpy as np  # noqa: E402
 # processes); absent until measured, and removed when the kernel changes.
 NCU_TRAFFIC_RATIO = {"splitk": 1.0011}  # profiles/splitk_partial_decode_b2h32_nq4_nk131072.md
 # For tensor-bound kernels: measured DRAM bytes per unmasked (query, key) pair.
-NCU_TRAFFIC_PER_PAIR = {"fwd": 0.0321, "bwd_fused": 0.0750}  # profiles/fwd_tc_b1h4_n65536_causal.md, profiles/bwd_fused_b1h4_n65536_causal.md
+NCU_TRAFFIC_PER_PAIR = {"fwd": 0.0321, "bwd_fused": 0.0740}  # profiles/fwd_tc_b1h4_n65536_causal.md, profiles/bwd_fused_b1h4_n65536_causal.md
 
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -59,6 +59,9 @@ def parse():
                          "setting")
     ap.add_argument("--nonsplit", action="store_true", help="decode workloads: time the non-split forward")
     ap.add_argument("--mutual", action="store_true", help="both settings' gradients (Q1, K1, Q2, K2 all train)")
+    ap.add_argument("--split-separate", action="store_true",
+                    help="separate path: launch the dQ and the dK kernels one after the other (per-kernel times and "
+                         "profiles) instead of as one launch")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
@@ -403,7 +406,7 @@ def run_ours(args):
             return (kl,) + tuple(grads)
         bwd = skl.bwd_s1 if args.setting == 1 else skl.bwd_s2
         extra = () if args.setting == 1 else (kl,)
-        if mode == skl.BWD_SEPARATE:
+        if mode == skl.BWD_SEPARATE and args.split_separate:
             dq = bwd(a, b, c, d, l1, l2, *extra, g_, scale, causal, skl.BWD_DQ_ONLY)[0]
             if ev:
                 ev[2].record(stream)
@@ -437,10 +440,14 @@ def run_ours(args):
         else:
             key_ranges = None
             launches_per_step = 5
-    elif mode == skl.BWD_SEPARATE:
+    elif mode == skl.BWD_SEPARATE and args.split_separate:
         kernels = ["fwd", "bwd_dq", "bwd_dk"]
         algo = {"fwd": 4 * w.D * pairs, "bwd_dq": 6 * w.D * pairs, "bwd_dk": 6 * w.D * pairs}
         launches_per_step = 3
+    elif mode == skl.BWD_SEPARATE:
+        kernels = ["fwd", "bwd_separate", "none"]
+        algo = {"fwd": 4 * w.D * pairs, "bwd_separate": 12 * w.D * pairs}
+        launches_per_step = 2
     else:
         kernels = ["fwd", "bwd_fused", "none"]
         algo = {"fwd": 4 * w.D * pairs, "bwd_fused": 8 * w.D * pairs}

@@ -216,11 +216,14 @@ streamkl_status streamkl_bwd_workspace(streamkl_shape s, int bwd_mode, size_t* b
  * Which path AUTO takes (pure host rule, no device; 0 for an invalid shape or
  * num_sms <= 0): the fused path (over key ranges when N_K is long; see
  * streamkl_bwd_fused_plan), except the separate kernels when a head has at
- * most two 128-row query tiles and the fused path would need more than one key
- * range -- a key tile is then reused by at most two query tiles, and the
- * separate kernels' extra recompute costs less than the fused path's dK atomics
- * and per-range dQ round trips (the "separate kernels under contention" rule of
- * section 手法 2 "kernel fusion", with the threshold measured on GB300).
+ * most eight 128-row query tiles and the fused path would either need more
+ * than one key range or launch fewer blocks (B*H*query tiles) than num_sms --
+ * a key tile is then reused by few query tiles, the separate kernels' extra
+ * recompute costs less than the fused path's dK atomics and per-range dQ round
+ * trips, and the separate dK grid's many short blocks fill the SMs its few
+ * long dQ blocks leave free (the two grids run as one launch).  This is the
+ * "separate kernels under contention" rule of section 手法 2 "kernel fusion",
+ * with the thresholds measured on GB300.
  */
 int streamkl_bwd_select(streamkl_shape s, size_t l2_bytes, int num_sms);
 /*
@@ -262,9 +265,9 @@ streamkl_status streamkl_bwd_s2(const void* q1, const void* k1, const void* q2, 
  * L = sum_i g_i KL_i are setting 2's (dQ1, dK1) and setting 1's (dQ2, dK2).
  * bwd_mode:
  *   STREAMKL_BWD_SEPARATE  the mutual kernels: S1 and S2 of each tile pair are
- *                          rebuilt once and both dS tiles formed from them (a
- *                          dQ kernel, then a dK kernel, no atomics, no
- *                          workspace); dS1 and dS2 are bit-identical to the
+ *                          rebuilt once and both dS tiles formed from them
+ *                          (dQ blocks and dK blocks in one launch, no atomics,
+ *                          no workspace); dS1 and dS2 are bit-identical to the
  *                          single settings', and so are the four outputs to
  *                          those of streamkl_bwd_s2 / streamkl_bwd_s1 with
  *                          STREAMKL_BWD_SEPARATE.
@@ -286,11 +289,11 @@ streamkl_status streamkl_bwd_mutual(const void* q1, const void* k1, const void* 
                                     void* dq2, void* dk2, int bwd_mode, void* workspace,
                                     size_t workspace_bytes, void* stream);
 /*
- * AUTO's choice for the mutual case on a device with `l2_bytes` of L2 and
- * `num_sms` SMs (pure host rule): STREAMKL_BWD_SEPARATE (the mutual kernels)
- * when the fused path would need more than one key range and a head has at
- * most 16 query tiles of 128 rows, else STREAMKL_BWD_FUSED (a fused pass per
- * setting), measured on GB300.  0 for an invalid shape.
+ * AUTO's choice for the mutual case (pure host rule; the arguments match
+ * streamkl_bwd_select's): STREAMKL_BWD_SEPARATE (the mutual kernels) when a
+ * head has at most 64 query tiles of 128 rows, else STREAMKL_BWD_FUSED (a
+ * fused pass per setting) -- the threshold measured on GB300.  0 for an
+ * invalid shape or num_sms <= 0.
  */
 int streamkl_bwd_mutual_select(streamkl_shape s, size_t l2_bytes, int num_sms);
 /* Workspace bytes streamkl_bwd_mutual needs in `bwd_mode` on the current device (0 for the mutual kernels). */

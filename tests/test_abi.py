@@ -184,8 +184,15 @@ def test_bwd_select_and_fused_plan(lib):
     # at most two query tiles per head and several key ranges: the separate kernels
     assert K.bwd_select(1, 128, 128, 65536, 128, l2, sms) == K.BWD_SEPARATE
     assert K.bwd_select(1, 64, 256, 131072, 128, l2, sms) == K.BWD_SEPARATE
-    assert K.bwd_select(1, 32, 512, 262144, 128, l2, sms) == K.BWD_FUSED  # four query tiles
-    assert K.bwd_select(1, 1, 128, 128, 64, l2, sms) == K.BWD_FUSED  # one key range
+    assert K.bwd_select(1, 32, 512, 262144, 128, l2, sms) == K.BWD_SEPARATE  # four query tiles
+    assert K.bwd_select(1, 8, 1024, 65536, 128, l2, sms) == K.BWD_SEPARATE  # eight
+    assert K.bwd_select(1, 8, 1025, 65536, 128, l2, sms) == K.BWD_FUSED  # nine
+    assert K.bwd_select(1, 8, 2048, 65536, 128, l2, sms) == K.BWD_FUSED
+    # one key range: the separate path only while the fused grid (B*H*query tiles blocks) leaves SMs idle
+    assert K.bwd_select(1, 1, 128, 128, 64, l2, sms) == K.BWD_SEPARATE
+    assert K.bwd_select(1, 18, 1024, 1024, 128, l2, sms) == K.BWD_SEPARATE  # 144 fused blocks on 152 SMs
+    assert K.bwd_select(1, 19, 1024, 1024, 128, l2, sms) == K.BWD_FUSED  # 152
+    assert K.bwd_select(64, 32, 1024, 1024, 128, l2, sms) == K.BWD_FUSED
     assert K.bwd_select(0, 1, 8, 8, 64, l2, sms) == 0  # invalid shape
     assert K.bwd_select(1, 1, 8, 8, 64, l2, 0) == 0  # no SM count
     # one launch while the live dK rows (heads in flight x N_K x D x 4 B) fit in L2
@@ -288,18 +295,16 @@ def test_key_shard_entry_points_validate_before_any_launch(lib):
 
 
 def test_bwd_mutual_select(lib):
-    """The mutual case: the mutual kernels where the fused path needs several key ranges and a head has at
-    most 16 query tiles; a fused pass per setting otherwise."""
+    """The mutual case: the mutual kernels while a head has at most 64 query tiles; a fused pass per setting
+    otherwise."""
     l2, sms = 135528448, 152  # GB300
     S = lambda *a: K.bwd_mutual_select(*a, l2, sms)  # noqa: E731
     assert S(1, 32, 128, 65536, 128) == K.BWD_SEPARATE
-    assert S(1, 8, 1024, 65536, 128) == K.BWD_SEPARATE  # 8 query tiles, 5 key ranges
-    assert S(1, 8, 2048, 262144, 128) == K.BWD_SEPARATE  # 16 query tiles
-    assert S(1, 8, 2049, 262144, 128) == K.BWD_FUSED  # 17 query tiles
-    assert S(1, 32, 65536, 65536, 128) == K.BWD_FUSED  # one key range
-    assert S(2, 32, 4096, 4096, 128) == K.BWD_FUSED
-    assert S(1, 8, 524288, 524288, 128) == K.BWD_FUSED  # many query tiles
-    assert K.bwd_fused_plan(1, 8, 1024, 65536, 128, l2, sms, False)[0] > 1
+    assert S(1, 8, 8192, 65536, 128) == K.BWD_SEPARATE  # 64 query tiles
+    assert S(1, 8, 8193, 65536, 128) == K.BWD_FUSED  # 65
+    assert S(2, 32, 4096, 4096, 128, True) == K.BWD_SEPARATE
+    assert S(1, 32, 65536, 65536, 128, True) == K.BWD_FUSED
+    assert S(1, 8, 524288, 524288, 128, True) == K.BWD_FUSED
     assert K.bwd_mutual_select(0, 1, 8, 8, 64, l2, sms) == 0
     assert K.bwd_mutual_select(1, 1, 8, 8, 64, l2, 0) == 0
 
