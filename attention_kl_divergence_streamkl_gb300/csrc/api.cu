@@ -180,9 +180,11 @@ size_t fused_workspace_bytes(const Problem& p, int range_tiles) {
 // blocks, fills the SMs that its few long dQ blocks leave free, both grids in
 // one launch (the "separate kernels under contention" rule of the technical
 // summary, section 手法 2 "kernel fusion").
-// Measured on B1 H8 N_K=64K non-causal, ms for setting 1's backward, separate
-// against fused: N_Q=512 0.71 / 1.24, N_Q=1024 0.76 / 1.24, N_Q=2048 1.39 /
-// 1.25, N_Q=4096 2.64 / 2.33; B1 H32 N_Q=128 N_K=64K 0.84 / 1.74.
+// Measured, ms for setting 1's backward, separate against fused: B1 H8
+// N_K=64K non-causal N_Q=256 0.70 / 1.16, N_Q=512 0.71 / 1.16, N_Q=1024 0.76 /
+// 1.17, N_Q=2048 1.39 / 1.25, N_Q=4096 2.64 / 2.33; B1 H32 N_Q=128 N_K=64K 0.84 /
+// 1.74; one key range: B1 H32 N_Q=512 N_K=4096 causal (128 fused blocks) 0.13 /
+// 0.17, B1 H32 N_Q=1024 N_K=8192 (256 fused blocks) 0.40 / 0.32.
 constexpr int kSeparateMaxQTiles = 8;
 int resolve_bwd_mode(const Problem& p, int mode, size_t l2_bytes, int num_sms) {
   if (mode != STREAMKL_BWD_AUTO) return mode;
@@ -197,11 +199,11 @@ int resolve_bwd_mode(const Problem& p, int mode, size_t l2_bytes, int num_sms) {
 // (one recompute of each logit tile pair for both settings, reported as
 // STREAMKL_BWD_SEPARATE) when a head has at most kMutualMaxQTiles query tiles,
 // else one fused pass per setting.  Measured, ms for both settings' backward
-// (mutual against two fused passes): B1 H32 N_Q=128 N_K=64K non-causal 1.16 /
-// 3.52; B1 H8 N_K=64K non-causal N_Q=1024 1.16 / 2.50, N_Q=4096 4.13 / 4.69,
-// N_Q=8192 8.11 / 8.82; causal B2 H32 N4096 1.23 / 1.30, B1 H8 N8K 0.62 / 0.68,
-// N16K 2.15 / 2.10, N32K 8.10 / 7.65, N64K 31.9 / 30.3; B1 H4 N64K non-causal
-// 31.9 / 30.6; B1 H2 N512K causal 508 / 492.
+// (mutual against two fused passes): B1 H32 N_Q=128 N_K=64K non-causal 1.15 /
+// 3.52; B1 H8 N_K=64K non-causal N_Q=1024 1.10 / 2.33, N_Q=8192 7.63 / 8.36,
+// N_Q=16384 15.1 / 14.6; causal B2 H32 N4096 1.18 / 1.25 (non-causal 2.08 /
+// 2.08), B1 H8 N8K 0.59 / 0.65, N16K 2.02 / 1.99, N32K 7.60 / 7.25, N64K 29.9 /
+// 29.0; B1 H2 N512K causal 508 / 492.
 constexpr int kMutualMaxQTiles = 64;
 int resolve_mutual_mode(const Problem& p, int mode, size_t l2_bytes, int num_sms) {
   (void)l2_bytes;

@@ -23,7 +23,8 @@
 // go through one 5-slot ring in the order K1(0), K2(0), K1(1), ...
 //   warps 0-15  dS warps: thread = query row (lane quarter = warp % 4), group g = warp / 4
 //               takes key columns [32g, 32g + 32); at the end they write dQ1 and dQ2
-//   warp 16     TMA producer        warp 17  TMEM owner and MMA issuer
+//   warp 16     TMA producer        warp 17  TMEM owner, issuer of the logits MMAs
+//   warp 18     issuer of the gradient MMAs: dQ1(j) at once, dQ2(j) once S2(j + 1) is queued
 //
 // dK blocks: a block owns 128 keys (K1, K2 stationary) and streams query tiles as
 // the M operand of the logits MMA, so a dS thread owns a query row:
@@ -33,7 +34,8 @@
 //                                         -> [256, 256 + D), [384, 384 + D)
 // Shared memory holds K1, K2, one dS buffer and a 4-slot ring of query tiles
 // (Q1(j), Q2(j), ...): the two query tiles of the tile being reduced and the
-// two of the next.  The dS warps store dS1, wait for its dK MMA, then store dS2.
+// two of the next.  The dS warps store dS1, copy S1 of the next tile while dK1's
+// MMA runs, then store dS2.
 //   warps 0-15  dS warps (then: thread = key row, group g = d columns [32g, 32g + 32) of dK1, dK2)
 //   warp 16     TMA producer        warp 17  TMEM owner and MMA issuer
 #include "common.cuh"
@@ -47,6 +49,7 @@ namespace {
 constexpr int DS_WARPS = 16;
 constexpr int PRODUCER_WARP = 16;
 constexpr int MMA_WARP = 17;
+constexpr int GRAD_WARP = 18;  // dQ blocks: issuer of the gradient MMAs
 constexpr int THREADS = 20 * 32;
 constexpr int kRegsDs = 104, kRegsOther = 64;  // 512 * 104 + 128 * 64 = 640 * 96 registers at launch
 constexpr uint32_t kTmemCols = 512;
@@ -95,9 +98,9 @@ struct Smem {
   static constexpr int OFF_X2 = TILE;
   static constexpr int OFF_Y = 2 * TILE;  // key-tile ring [SLOTS]
   static constexpr int OFF_BAR = OFF_Y + SLOTS * TILE;
-  // x_full, y_full[5], y_empty[5], s_full, s_free, ds_full, ds_free, g_done; then the TMEM base address slot
-  // and the abort flag
-  static constexpr int BAR_SLOT = 8 * 16;
+  // x_full, y_full[5], y_empty[5], s_full, s_free, ds_full, ds_free, g_done, s2_issued; then the TMEM base
+  // address slot and the abort flag
+  static constexpr int BAR_SLOT = 8 * 17;
   static constexpr int BYTES = OFF_BAR + BAR_SLOT + 16 + 1024;
 };
 static_assert(Smem<128>::BYTES <= 227 * 1024, "shared memory");
@@ -129,11 +132,13 @@ __device__ __forceinline__ void dq_mutual_block(const Problem& p, const float* _
 
   const uint32_t bar = sb + L::OFF_BAR;
   const uint32_t x_full = bar, y_full = bar + 8, y_empty = bar + 48, s_full = bar + 88, s_free = bar + 96,
-                 ds_full = bar + 104, ds_free = bar + 112, g_done = bar + 120, slot = bar + L::BAR_SLOT;
+                 ds_full = bar + 104, ds_free = bar + 112, g_done = bar + 120, s2_issued = bar + 128,
+                 slot = bar + L::BAR_SLOT;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_BAR + L::BAR_SLOT + 4);
 
   if (threadIdx.x == 0) {
     mbar_init(x_full, 1);
+    mbar_init(s2_issued, 1);
     for (int s = 0; s < SLOTS; ++s) {
       mbar_init(y_full + 8 * s, 1);
       mbar_init(y_empty + 8 * s, 1);
@@ -184,55 +189,63 @@ __device__ __forceinline__ void dq_mutual_block(const Problem& p, const float* _
       }
       __syncwarp();
     } else if (warp == MMA_WARP) {
-      // ------------------------------------------------------------------ MMA issuer
+      // ------------------------------------------------------------------ MMA issuer: logits
+      // S1(j) once the dS warps have copied S2(j - 1) out of the region, S2(j) once they hold S1(j);
+      // s_free completes twice per key tile: S1(j) copied (2j), S2(j) copied (2j + 1)
       if (lane == 0) {
         constexpr uint32_t id_s = idesc_bf16(BX, BY, false, false);
-        constexpr uint32_t id_g = idesc_bf16(BX, D, false, true);
         const uint64_t x1d = sdesc_sw128(sb + L::OFF_X1, 0, 1024), x2d = sdesc_sw128(sb + L::OFF_X2, 0, 1024);
         bool ok = mbar_wait(x_full, 0, status, abort_flag);
-        // s_free completes twice per key tile: S1(j) copied (2j), S2(j) copied (2j + 1)
-        for (int j = 0; ok && j <= n_yt; ++j) {
-          if (j < n_yt) {
+        for (int i = 0; ok && i < n_items; ++i) {
+          const int t = i & 1, s = i % SLOTS;
+          if (!mbar_wait(y_full + 8 * s, (i / SLOTS) & 1, status, abort_flag)) break;
+          if (i >= 1 && !mbar_wait(s_free, (i - 1) & 1, status, abort_flag)) break;
+          tc_fence_after();
+          const uint64_t xd = t ? x2d : x1d;
+          const uint64_t yd = sdesc_sw128(sb + L::OFF_Y + s * L::TILE, 0, 1024);
 #pragma unroll
-            for (int t = 0; t < 2; ++t) {
-              const int i = 2 * j + t, s = i % SLOTS;
-              if (!mbar_wait(y_full + 8 * s, (i / SLOTS) & 1, status, abort_flag)) {
-                ok = false;
-                break;
-              }
-              if (i >= 1 && !mbar_wait(s_free, (i - 1) & 1, status, abort_flag)) {
-                ok = false;
-                break;
-              }
-              tc_fence_after();
-              const uint64_t xd = t ? x2d : x1d;
-              const uint64_t yd = sdesc_sw128(sb + L::OFF_Y + s * L::TILE, 0, 1024);
-#pragma unroll
-              for (int ks = 0; ks < D / 16; ++ks) {
-                const uint32_t off = (ks >> 2) * (128 * 128) + (ks & 3) * 32;  // BX == BY: same half stride
-                mma_ss(tmem + kColS, sdesc_add(xd, off), sdesc_add(yd, off), id_s, ks > 0);
-              }
-              mma_commit(s_full);
-            }
-            if (!ok) break;
+          for (int ks = 0; ks < D / 16; ++ks) {
+            const uint32_t off = (ks >> 2) * (128 * 128) + (ks & 3) * 32;  // BX == BY: same half stride
+            mma_ss(tmem + kColS, sdesc_add(xd, off), sdesc_add(yd, off), id_s, ks > 0);
           }
-          if (j >= 1) {
-            const int jj = j - 1;
-            if (!mbar_wait(ds_full, jj & 1, status, abort_flag)) break;
+          mma_commit(s_full);
+          if (t) mbar_arrive(s2_issued);  // S2(j) is in the tensor pipe's queue
+        }
+      }
+      __syncwarp();
+    } else if (warp == GRAD_WARP) {
+      // ------------------------------------------------------------------ MMA issuer: gradients
+      // dQ1(j) as soon as dS(j) is in TMEM, so it runs while the dS warps copy S1(j + 1); dQ2(j) once
+      // S2(j + 1) is queued, so the logits the dS warps wait for come first (pipe order S1(j + 1),
+      // dQ1(j), S2(j + 1), dQ2(j)).
+      if (lane == 0) {
+        constexpr uint32_t id_g = idesc_bf16(BX, D, false, true);
+        bool ok = true;
+        for (int j = 0; ok && j < n_yt; ++j) {
+          if (!mbar_wait(ds_full, j & 1, status, abort_flag)) break;
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            const int i = 2 * j + t, s = i % SLOTS;
+            if (t && j + 1 < n_yt && !mbar_wait(s2_issued, (j + 1) & 1, status, abort_flag)) {
+              ok = false;
+              break;
+            }
+            // K_t(j) has landed (its logits MMA read it); waited here too so that this thread's MMAs are
+            // ordered after the copy
+            if (!mbar_wait(y_full + 8 * s, (i / SLOTS) & 1, status, abort_flag)) {
+              ok = false;
+              break;
+            }
             tc_fence_after();
+            // A = dS_t packed in TMEM (16 keys = 8 columns per k-step); B = K_t read MN-major
+            const uint64_t yd = sdesc_sw128(sb + L::OFF_Y + s * L::TILE, BY * 128, 1024);
+            const uint32_t g_col = t ? kColG2 : kColG1, ds_col = t ? kColDS2 : kColDS1;
 #pragma unroll
-            for (int t = 0; t < 2; ++t) {
-              const int i = 2 * jj + t, s = i % SLOTS;
-              // A = dS_t packed in TMEM (16 keys = 8 columns per k-step); B = K_t read MN-major
-              const uint64_t yd = sdesc_sw128(sb + L::OFF_Y + s * L::TILE, BY * 128, 1024);
-              const uint32_t g_col = t ? kColG2 : kColG1, ds_col = t ? kColDS2 : kColDS1;
-#pragma unroll
-              for (int ks = 0; ks < BY / 16; ++ks)
-                mma_ts(tmem + g_col, tmem + ds_col + 8 * ks, sdesc_add(yd, ks * 2048), id_g, jj > 0 || ks > 0);
-              mma_commit(y_empty + 8 * s);
-            }
-            mma_commit(ds_free);
+            for (int ks = 0; ks < BY / 16; ++ks)
+              mma_ts(tmem + g_col, tmem + ds_col + 8 * ks, sdesc_add(yd, ks * 2048), id_g, j > 0 || ks > 0);
+            mma_commit(y_empty + 8 * s);
           }
+          if (ok) mma_commit(ds_free);
         }
         mma_commit(g_done);
         mbar_drain(g_done, 0, status);
@@ -520,22 +533,27 @@ __device__ __forceinline__ void dk_mutual_block(const Problem& p, const float* _
       __syncwarp();
       if (lane == 0) mbar_arrive(ds_full);
     };
-    RowVals v = fetch(0);
-    bool ok = true;
-    for (int j = 0; j < n_qt; ++j) {
-      const RowVals vn = fetch(j + 1);
-      const int q = q_begin + j * BQ + r;
-      ok = mbar_wait_warp(sa_full, j & 1, status, abort_flag);
+    // S1(j) is copied out before the loop body of tile j: for j >= 1 while dK1(j - 1)'s MMA, which the
+    // dS warps wait for before they can store dS2(j - 1), is running
+    uint32_t s1[32];  // this thread's 32 columns of S1 of the current tile
+    auto copy_s1 = [&](int j) {
+      const bool got = mbar_wait_warp(sa_full, j & 1, status, abort_flag);
       __syncwarp();
-      if (!ok) break;
+      if (!got) return false;
       tc_fence_after();
-      uint32_t s1[32];  // this thread's 32 columns of S1
       tmem_ld32(tcol + kColSA, s1);
       tmem_ld_wait();
       reg_fence32(s1);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(sa_free);
+      return true;
+    };
+    RowVals v = fetch(0);
+    bool ok = n_qt > 0 && copy_s1(0);
+    for (int j = 0; ok && j < n_qt; ++j) {
+      const RowVals vn = fetch(j + 1);
+      const int q = q_begin + j * BQ + r;
       const int kg = k0 + grp * 32;
       const bool masked = (kg + 31 >= p.NK) || (q >= p.NQ) || (p.causal && kg + 31 > q + p.off);
       ok = mbar_wait_warp(sb_full, j & 1, status, abort_flag);
@@ -570,6 +588,7 @@ __device__ __forceinline__ void dk_mutual_block(const Problem& p, const float* _
         if (!ok) break;
       }
       store_ds(pk1);
+      if (j + 1 < n_qt && !(ok = copy_s1(j + 1))) break;  // S1(j + 1) was issued before dK1(j)
       ok = mbar_wait_warp(ds_free, 0, status, abort_flag);  // completion 2j: dK1 of tile j done
       __syncwarp();
       if (!ok) break;
