@@ -462,6 +462,27 @@ def run_ours(args):
     torch.cuda.synchronize(dev)
     assert skl.check_device_status(dev) == 0, "device-side timeout during warm-up"
 
+    # ---- extra HBM of one step (outside the timed region): the allocator's peak during the step minus what was
+    # allocated before it (the inputs) and minus the step's outputs (KL, LSE1, LSE2 and the gradients)
+    torch.cuda.synchronize(dev)
+    torch.cuda.reset_peak_memory_stats(dev)
+    before = torch.cuda.memory_allocated(dev)
+    outs = step((q1, k1, q2, k2))
+    torch.cuda.synchronize(dev)
+    peak = torch.cuda.max_memory_allocated(dev)
+    rows = w.B * w.H * w.NQ * 4
+    # a decode step returns KL, LSE1, LSE2; a training step KL and the gradients (its LSE1, LSE2 are outputs of
+    # the forward too, freed when the step returns)
+    out_bytes = sum(t.numel() * t.element_size() for t in outs if t is not None) + (0 if decode else 2 * rows)
+    extra_bytes = max(0, peak - before - out_bytes)
+    del outs
+    p_bytes = 2 * w.unmasked_pairs() * 2 if not decode else 2 * w.B * w.H * w.NQ * w.NK * 2
+    extra_hbm = {"bytes": int(extra_bytes), "peak_bytes": int(peak), "inputs_bytes": int(before),
+                 "outputs_bytes": int(out_bytes), "materialised_p1_p2_bf16_bytes": int(p_bytes),
+                 "materialised_over_extra": (p_bytes / extra_bytes) if extra_bytes else None,
+                 "note": "the fused backward's fp32 dK accumulator (and, over key ranges, the fp32 dQ sum) is the "
+                         "workspace; a path that materialises P1 and P2 holds at least the bf16 bytes given"}
+
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(gpu_id_for(local))
@@ -596,6 +617,7 @@ def run_ours(args):
                        "l2": "inputs larger than L2, no flush between steps",
                        "parallelism": f"replicas{world}"},
             "roofline": roof, "per_kernel_ms": {k: v / args.steps for k, v in per_kernel.items()},
+            "extra_hbm": extra_hbm,
             "gpu_launches": launches_per_step * args.steps, "clocks": clocks, "e2e": e2e, "cpu_baseline": cpu}
     if decode_section is not None:
         line["decode"] = decode_section
