@@ -181,7 +181,7 @@ def test_bwd_select_and_fused_plan(lib):
     l2, sms = 135528448, 152  # GB300
     assert K.bwd_select(1, 8, 524288, 524288, 128, l2, sms) == K.BWD_FUSED  # many query tiles: fused over ranges
     assert K.bwd_select(1, 32, 65536, 65536, 128, l2, sms, True) == K.BWD_FUSED
-    # at most two query tiles per head and several key ranges: the separate kernels
+    # at most eight query tiles per head and several key ranges: the separate kernels
     assert K.bwd_select(1, 128, 128, 65536, 128, l2, sms) == K.BWD_SEPARATE
     assert K.bwd_select(1, 64, 256, 131072, 128, l2, sms) == K.BWD_SEPARATE
     assert K.bwd_select(1, 32, 512, 262144, 128, l2, sms) == K.BWD_SEPARATE  # four query tiles
