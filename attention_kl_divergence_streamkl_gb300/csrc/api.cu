@@ -71,6 +71,10 @@ streamkl_status validate(const streamkl_shape& s, Problem* p) {
   if ((long long)s.B * s.H > 0x7fffffffLL) return STREAMKL_ERR_UNSUPPORTED;
   if (s.D != 64 && s.D != 128) return STREAMKL_ERR_UNSUPPORTED;
   if ((s.NQ + 127LL) / 128 > kMaxGridY || (s.NK + 127LL) / 128 > kMaxGridY) return STREAMKL_ERR_UNSUPPORTED;
+  // one-dimensional grids of (query tiles + key tiles) blocks per head must fit a grid's x extent (and the
+  // kernels' int block arithmetic)
+  if ((long long)s.B * s.H * ((s.NQ + 127LL) / 128 + (s.NK + 127LL) / 128) > 0x7fffffffLL)
+    return STREAMKL_ERR_UNSUPPORTED;
   p->B = s.B;
   p->H = s.H;
   p->NQ = s.NQ;

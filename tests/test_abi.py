@@ -65,6 +65,9 @@ def call_fwd(lib, shape, q=None, kl=None):
     (dict(B=1, H=1, NQ=8, NK=8, D=64, scale=float("inf")), K.ERR_INVALID),
     (dict(B=1, H=1, NQ=8, NK=2**31 - 1, D=64), K.ERR_UNSUPPORTED),
     (dict(B=65536, H=65536, NQ=8, NK=8, D=64), K.ERR_UNSUPPORTED),
+    # B*H fits, but (query tiles + key tiles) x B*H blocks would not fit a grid
+    (dict(B=1 << 15, H=1 << 15, NQ=256, NK=256, D=64), K.ERR_UNSUPPORTED),
+    (dict(B=1, H=1 << 21, NQ=65536, NK=65536, D=64), K.ERR_UNSUPPORTED),
 ])
 def test_fwd_rejects_bad_shapes_before_launch(lib, shape, code):
     assert call_fwd(lib, K.make_shape(**shape)) == code
