@@ -246,6 +246,18 @@ __global__ void wait_timeout_probe_kernel(unsigned long long limit_ns, int* stat
 
 }  // namespace
 
+bool encode_rows_f32_map(CUtensorMap* map, float* base, int D, int rows, int BH, int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)rows, (cuuint64_t)BH};
+  const cuuint64_t strides[2] = {(cuuint64_t)D * 4, (cuuint64_t)rows * D * 4};
+  const cuuint32_t box[3] = {(cuuint32_t)D, (cuuint32_t)box_rows, 1u};
+  const cuuint32_t estr[3] = {1u, 1u, 1u};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool encode_tile_map(CUtensorMap* map, const void* base, int D, int N, int H, int B, long long sn, long long sh,
                      long long sb, int box_rows) {
   EncodeTiledFn fn = encode_fn();

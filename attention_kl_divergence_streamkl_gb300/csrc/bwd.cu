@@ -17,7 +17,8 @@
 //   dS from S and the row's folded LSE1, LSE2, g, KL; to smem as dS[query][key]
 //   dQ   += dS K_opt                    SS: A = dS (K-major over keys), B = K_opt MN-major  -> [128, 128 + D)
 //   dKp^T = Q_opt^T dS                  SS: A = Q_opt read MN-major (M = d), B = dS MN-major -> [256 + 128 b, ...)
-//   dk_acc[key, d] += dKp^T[d, key]     one warp adds 32 consecutive d of one key row (128 B) per red
+//   dk_acc[key, d] += dKp^T[d, key]     staged in smem 32 keys at a time, added by a TMA bulk tensor
+//                                       reduction (cp.reduce.async.bulk.tensor .add.f32)
 // Two threads issue the MMAs, each from its own warp: one the logits S_a(j),
 // S_b(j) of every key tile, the other the gradient MMAs dQ(j), dKp(j) once dS(j)
 // is in shared memory.  A tcgen05.mma takes a single issuing thread several
@@ -30,21 +31,27 @@
 // The dS warps copy S_a into registers (in setting 1 they turn it into P1 while
 // S_b is in flight), S_b is written over it and read in two halves.  A thread
 // owns a query row, so its per-query values sit in registers
-// and the dS loop issues no shared-memory loads; the dK warps' reductions,
-// bounded by L2 reduction throughput, overlap it instead of competing for the
-// LSU.  dKp^T is double-buffered so they have two tile periods per tile.
+// and the dS loop issues no shared-memory loads.  dKp^T is double-buffered so
+// the dK warps have two tile periods per tile.  They read it from TMEM, write
+// each 32-key chunk into a shared buffer as [key][d] fp32 and one thread adds
+// the chunk into the fp32 accumulator with a TMA bulk reduction: 64 KB of
+// dK partial per tile would otherwise take 512 warp-wide red.global
+// instructions through the load/store path, which measured 14% of the kernel
+// (a timing-only copy without them ran B1 H32 N64K causal in 50.6 against
+// 59.4 ms; plain stores in their place cost as much as the reductions).  The
+// chunk buffers take the second slot of the other K tile's ring (B1 H32:
+// 59.4 -> 58.1 ms; setting 2 at H8 14.87 -> 14.16).
 //   warps 0-15  dS warps: thread = query row (lane quarter = warp % 4), group g = warp / 4
 //               takes key columns [32g, 32g + 32); at the end they write dQ
-//   warp 16     TMA producer: Q1, Q2 once, the other K tile through two slots
+//   warp 16     TMA producer: Q1, Q2 once, the other K tile through one slot
 //   warp 17     TMEM owner and issuer of the logits MMAs
 //   warp 18     TMA producer of K_opt (two slots, each held until the gradient MMAs)
 //   warp 19     issuer of the gradient MMAs
 //   warps 20-27 dK warps: thread = column d of dKp^T (lane quarter = warp % 4), warps
-//               20-23 take keys [0, 64) of a tile and 24-27 keys [64, 128); they
-//               reduce-add into dk_acc (two per SMSP keep more reductions in flight)
+//               20-23 take keys [0, 64) of a tile and 24-27 keys [64, 128), each group
+//               with its own 16 KB chunk buffer
 // Warpgroups 4-6 give registers to the dS warpgroups (setmaxnreg).
 #include <algorithm>
-#include <utility>
 
 #include "common.cuh"
 #include "ds_math.cuh"
@@ -56,7 +63,9 @@ namespace {
 
 constexpr int BQ = 128;  // queries per block (M of the S and dQ MMAs)
 constexpr int BK = 128;  // keys per step (N of the S and dKp MMAs)
-constexpr int SLOTS = 2;  // per streamed K tensor
+constexpr int SLOTS = 2;     // K_opt slots
+constexpr int KT_SLOTS = 1;  // slots of the other K tile
+constexpr int STG_ROWS = 32; // keys per staged dK chunk
 constexpr int DS_WARPS = 16;
 constexpr int PRODUCER_WARP = 16;
 constexpr int MMA_WARP = 17;
@@ -77,7 +86,9 @@ struct Smem {
   static constexpr int OFF_Q2 = TQ;
   static constexpr int OFF_KO = 2 * TQ;              // K_opt slots
   static constexpr int OFF_KT = OFF_KO + SLOTS * TK;  // the other K tile's slots
-  static constexpr int OFF_DS = OFF_KT + SLOTS * TK;  // dS[query][key] bf16: 2 halves of [128 queries][128 B]
+  static constexpr int STG = STG_ROWS * D * 4;        // one staged dK chunk: [32 keys][D] fp32
+  static constexpr int OFF_STG = OFF_KT + KT_SLOTS * TK;  // two chunk buffers (one per dK warp group)
+  static constexpr int OFF_DS = OFF_STG + 2 * STG;    // dS[query][key] bf16: 2 halves of [128 queries][128 B]
   static constexpr int DS_BYTES = BQ * BK * 2;
   static constexpr int OFF_BAR = OFF_DS + DS_BYTES;
   // mbarriers (8 B each): q_full, ko_full[2], ko_empty[2] (S_b and dQ both arrive), kt_full[2],
@@ -93,19 +104,6 @@ __device__ __forceinline__ void setmaxnreg_inc_ds() {
 }
 __device__ __forceinline__ void setmaxnreg_dec_other() {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsOther));
-}
-
-// red.global.add.f32 at base + OFF bytes: the offset rides in the instruction,
-// so a row loop keeps one 64-bit address live instead of one per row.
-template <int OFF>
-__device__ __forceinline__ void red_add_at(float* base, float a) {
-  asm volatile("red.global.add.f32 [%0+%2], %1;" ::"l"(base), "f"(a), "n"(OFF) : "memory");
-}
-// base[i * D] += v[i] for the rows i < nrow of a 32-row block
-template <int D, int... I>
-__device__ __forceinline__ void red_rows(float* base, const uint32_t (&v)[32], int nrow,
-                                         std::integer_sequence<int, I...>) {
-  ((I < nrow ? red_add_at<I * D * 4>(base, __uint_as_float(v[I])) : void()), ...);
 }
 
 // One launch covers the key tiles [jt0, jt1) and the query tiles from qt_min on
@@ -126,7 +124,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                         const float* __restrict__ gv, __nv_bfloat16* __restrict__ dq_out,
                         float* __restrict__ dk_acc, int* status,
                         const __grid_constant__ CUtensorMap mq1, const __grid_constant__ CUtensorMap mq2,
-                        const __grid_constant__ CUtensorMap mk1, const __grid_constant__ CUtensorMap mk2) {
+                        const __grid_constant__ CUtensorMap mk1, const __grid_constant__ CUtensorMap mk2,
+                        const __grid_constant__ CUtensorMap mdk) {
   using L = Smem<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
@@ -199,8 +198,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         const CUtensorMap* mka = SETTING == 1 ? &mk1 : &mk2;
         int issued = 0;
         for (int j = 0; j < n_kt; ++j) {
-          const int s = j % SLOTS;
-          if (j >= SLOTS && !mbar_wait(kt_empty + 8 * s, ((j / SLOTS) - 1) & 1, status, abort_flag)) break;
+          const int s = j % KT_SLOTS;
+          if (j >= KT_SLOTS && !mbar_wait(kt_empty + 8 * s, ((j / KT_SLOTS) - 1) & 1, status, abort_flag)) break;
           mbar_arrive_expect_tx(kt_full + 8 * s, L::TK);
 #pragma unroll
           for (int h = 0; h < D / 64; ++h)
@@ -209,8 +208,8 @@ __global__ void __launch_bounds__(THREADS, 1)
           issued = j + 1;
         }
         mbar_drain(q_full, 0, status);
-        for (int j = max(0, issued - SLOTS); j < issued; ++j)
-          mbar_drain(kt_full + 8 * (j % SLOTS), (j / SLOTS) & 1, status);
+        for (int j = max(0, issued - KT_SLOTS); j < issued; ++j)
+          mbar_drain(kt_full + 8 * (j % KT_SLOTS), (j / KT_SLOTS) & 1, status);
       }
       __syncwarp();
     } else if (warp == KOPT_WARP) {
@@ -243,18 +242,18 @@ __global__ void __launch_bounds__(THREADS, 1)
         const uint64_t qad = sdesc_sw128(sb + OFF_QA, 0, 1024), qbd = sdesc_sw128(sb + OFF_QB, 0, 1024);
         bool ok = mbar_wait(q_full, 0, status, abort_flag);
         for (int j = 0; ok && j < n_kt; ++j) {
-          const int s = j % SLOTS;
-          if (!mbar_wait(kt_full + 8 * s, (j / SLOTS) & 1, status, abort_flag)) break;
+          const int s = j % SLOTS, st = j % KT_SLOTS;
+          if (!mbar_wait(kt_full + 8 * st, (j / KT_SLOTS) & 1, status, abort_flag)) break;
           if (j >= 1 && !mbar_wait(sb_free, (j - 1) & 1, status, abort_flag)) break;
           tc_fence_after();
-          const uint64_t kad = sdesc_sw128(sb + L::OFF_KT + s * L::TK, 0, 1024);
+          const uint64_t kad = sdesc_sw128(sb + L::OFF_KT + st * L::TK, 0, 1024);
 #pragma unroll
           for (int ks = 0; ks < D / 16; ++ks) {
             const uint32_t off = (ks >> 2) * (128 * 128) + (ks & 3) * 32;  // BQ == BK: same half stride
             mma_ss(tmem + kColS, sdesc_add(qad, off), sdesc_add(kad, off), id_s, ks > 0);
           }
           mma_commit(sa_full);
-          mma_commit(kt_empty + 8 * s);  // the other K tile is read only by S_a
+          mma_commit(kt_empty + 8 * st);  // the other K tile is read only by S_a
           if (!mbar_wait(sa_free, j & 1, status, abort_flag)) break;
           if (!mbar_wait(ko_full + 8 * s, (j / SLOTS) & 1, status, abort_flag)) break;
           tc_fence_after();
@@ -317,19 +316,22 @@ __global__ void __launch_bounds__(THREADS, 1)
       __syncwarp();
     } else if (warp >= DK_WARP0) {
       // ------------------------------------------------------------------ dK warps
+      // Group h (warps 20-23: keys [0, 64) of a tile, warps 24-27: keys [64, 128)) stages each 32-key chunk of
+      // the dKp^T tile in its own shared buffer as [key][d] fp32 and one thread adds the chunk into dk_acc with
+      // a TMA bulk tensor reduction (rows past the range's end are clipped by the map).
       const int wq = (warp - DK_WARP0) & 3, half = (warp - DK_WARP0) >> 2;
       const int d = wq * 32 + lane;  // lane of dKp^T = column d
       const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
+      const uint32_t stg = sb + L::OFF_STG + half * L::STG;
+      const bool leader = wq == 0 && lane == 0;
       for (int j = 0; j < n_kt; ++j) {
         const int b = j & 1;
         const bool got = mbar_wait_warp(dk_full + 8 * b, (j >> 1) & 1, status, abort_flag);
-        __syncwarp();
-        if (!got) break;
+        // the group's four warps stop together (they share named barriers below)
+        if (named_bar_any(2 + half, 128, !got)) break;
         tc_fence_after();
-        const int k0 = kbase + j * BK;
-        float* base = dk_acc + ((size_t)bh * kr.dk_rows + j * BK) * D + d;
 #pragma unroll 1
-        for (int cb = 2 * half; cb < 2 * half + 2; ++cb) {  // this warp's half of the keys
+        for (int cb = 2 * half; cb < 2 * half + 2; ++cb) {  // this group's half of the keys
           uint32_t v[32];
           tmem_ld32(tmem + lane_base + kColDK + 128 * b + 32 * cb, v);
           tmem_ld_wait();
@@ -341,10 +343,27 @@ __global__ void __launch_bounds__(THREADS, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(dk_free + 8 * b);
           }
-          if (d < D)
-            red_rows<D>(base + (size_t)(32 * cb) * D, v, p.NK - k0 - 32 * cb, std::make_integer_sequence<int, 32>{});
+          // the group's buffer is free once the previous reduction from it has read it
+          if (leader) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+          named_bar_sync(2 + half, 128);
+          if (d < D) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              asm volatile("st.shared.f32 [%0], %1;" ::"r"(stg + (uint32_t)(i * D + d) * 4), "r"(v[i]) : "memory");
+          }
+          fence_async_smem();
+          named_bar_sync(2 + half, 128);
+          const int row0 = j * BK + 32 * cb;  // first accumulator row of the chunk within the head
+          if (leader && row0 < kr.dk_rows) {  // a chunk wholly past the range's rows has nothing to add
+            asm volatile(
+                "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%1, %2, %3}], [%4];"
+                ::"l"(reinterpret_cast<uint64_t>(&mdk)), "r"(0), "r"(row0), "r"(bh), "r"(stg)
+                : "memory");
+            asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+          }
         }
       }
+      if (leader) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
     }
   } else {
     setmaxnreg_inc_ds();
@@ -501,8 +520,11 @@ cudaError_t launch_fused(const Problem& p, const KeyRange& kr, const BwdIn& in, 
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const long long blocks = (long long)p.BH * ((p.NQ + BQ - 1) / BQ - kr.qt_min);
+  CUtensorMap mdk;
+  if (!encode_rows_f32_map(&mdk, dk_acc, D, kr.dk_rows, p.BH, STG_ROWS)) return cudaErrorInvalidValue;
   kern<<<(unsigned)blocks, THREADS, smem, st>>>(p, kr, in.lse1, in.lse2, in.kl, in.g,
-                                                static_cast<__nv_bfloat16*>(dq), dk_acc, status, mq1, mq2, mk1, mk2);
+                                                static_cast<__nv_bfloat16*>(dq), dk_acc, status, mq1, mq2, mk1, mk2,
+                                                mdk);
   return cudaGetLastError();
 }
 

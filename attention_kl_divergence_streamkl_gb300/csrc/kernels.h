@@ -29,6 +29,9 @@ __host__ __device__ inline long long row_offset(int bh, int H, long long n, long
 // swizzle.  Returns false if the driver rejects it.
 bool encode_tile_map(CUtensorMap* map, const void* base, int D, int N, int H, int B, long long sn, long long sh,
                      long long sb, int box_rows);
+// A 3-D TMA map {d, row, bh} over an fp32 [BH][rows][D] accumulator, a {D, box_rows, 1} box, no swizzle
+// (for bulk reductions into it).
+bool encode_rows_f32_map(CUtensorMap* map, float* base, int D, int rows, int BH, int box_rows);
 // The maps of Q1/Q2 and K1/K2 of a problem.
 inline bool encode_q_map(CUtensorMap* map, const void* base, const Problem& p, int box_rows) {
   return encode_tile_map(map, base, p.D, p.NQ, p.H, p.B, p.qs_n, p.qs_h, p.qs_b, box_rows);
