@@ -32,7 +32,7 @@ import numpy as np  # noqa: E402
 # processes); absent until measured, and removed when the kernel changes.
 NCU_TRAFFIC_RATIO = {"splitk": 1.0011}  # profiles/splitk_partial_decode_b2h32_nq4_nk131072.md
 # For tensor-bound kernels: measured DRAM bytes per unmasked (query, key) pair.
-NCU_TRAFFIC_PER_PAIR = {"fwd": 0.0321, "bwd_fused": 0.0747}  # profiles/fwd_tc_b1h4_n65536_causal.md, profiles/bwd_fused_b1h4_n65536_causal.md
+NCU_TRAFFIC_PER_PAIR = {"fwd": 0.0321, "bwd_fused": 0.0744}  # profiles/fwd_tc_b1h4_n65536_causal.md, profiles/bwd_fused_b1h4_n65536_causal.md
 
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
