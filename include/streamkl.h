@@ -199,9 +199,9 @@ streamkl_status streamkl_dq_from_partial(const float* dq_partial, streamkl_shape
 
 /*
  * Backward workspace for the current device (0 bytes for the separate path).
- * The fused path adds dK partials with fp32 atomics into an accumulator that
- * the library zeroes; they stay cheap while the rows being accumulated sit in
- * L2.  Its blocks run head by head, so the live rows are one head's keys times
+ * The fused path adds dK partials (TMA bulk fp32 reductions) into an
+ * accumulator that the library zeroes; they stay cheap while the rows being
+ * accumulated sit in L2.  Its blocks run head by head, so the live rows are one head's keys times
  * the heads a wave of blocks spans.  When all N_K keys fit that way, one
  * launch covers them and the workspace is the fp32 [B,H,N_K,D] dK accumulator
  * (dQ stays on chip).  Otherwise the keys are split into ranges whose live rows
