@@ -91,8 +91,8 @@ struct Smem {
   static constexpr int OFF_DS = OFF_STG + 2 * STG;    // dS[query][key] bf16: 2 halves of [128 queries][128 B]
   static constexpr int DS_BYTES = BQ * BK * 2;
   static constexpr int OFF_BAR = OFF_DS + DS_BYTES;
-  // mbarriers (8 B each): q_full, ko_full[2], ko_empty[2] (S_b and dQ both arrive), kt_full[2],
-  // kt_empty[2], sa_full, sa_free, sb_full, sb_free, ds_full, ds_free, dk_full[2], dk_free[2],
+  // mbarriers (8 B each): q_full, ko_full[2], ko_empty[2] (S_b and dQ both arrive), kt_full[2] and
+  // kt_empty[2] (the first KT_SLOTS used), sa_full, sa_free, sb_full, sb_free, ds_full, ds_free, dk_full[2], dk_free[2],
   // all_done, sb_issued; then the TMEM base address slot and the abort flag
   static constexpr int BAR_SLOT = 21 * 8;
   static constexpr int BYTES = OFF_BAR + BAR_SLOT + 16 + 1024;
