@@ -179,10 +179,12 @@ def gpu_id_for(dev_index: int) -> str:
 
 # ----------------------------------------------------------------------------- oracle (CPU) sample
 
-def oracle_sample(w, setting: int, target_s: float):
-    """Times the fp64 oracle's forward + backward on the last R query rows of head (0, 0).
+def oracle_sample(w, settings, target_s: float):
+    """Times the fp64 oracle's forward + the backward of each setting in `settings` on
+    the last R query rows of head (0, 0); a decode workload (no settings) runs all of
+    its query rows of that head and is counted in bytes of K1 and K2 read.
 
-    Returns (counted TFLOP/s, seconds, rows, description)."""
+    Returns (value in TFLOP/s, or GB/s for decode; seconds, rows, description)."""
     from attention_kl_divergence_streamkl_gb300 import synth
     from oracle import oracle as O
     q1, k1, q2, k2 = (synth.bf16_bits_to_f64(synth.head_slice(w, k, 0, 0)) for k in ("q1", "k1", "q2", "k2"))
@@ -191,8 +193,18 @@ def oracle_sample(w, setting: int, target_s: float):
     def run(rows):
         t0 = time.perf_counter()
         O.rows_forward(q1, k1, q2, k2, w.softmax_scale, w.causal, rows)
-        O.head_backward_rows(setting, q1, k1, q2, k2, w.softmax_scale, w.causal, g, rows)
+        for setting in settings:
+            O.head_backward_rows(setting, q1, k1, q2, k2, w.softmax_scale, w.causal, g, rows)
         return time.perf_counter() - t0
+
+    if not settings:
+        rows = np.arange(w.NQ)
+        reps = max(1, int(min(target_s, 2.0) / max(run(rows), 1e-6)))
+        dt = sum(run(rows) for _ in range(reps))
+        nbytes = 2 * w.NK * w.D * 2 + 2 * w.NQ * w.D * 2
+        desc = (f"fp64 oracle forward on all {w.NQ} query rows of head (0,0) against its {w.NK} keys, {reps} times "
+                f"({nbytes} bytes of K1, K2, Q1 and Q2 in bf16 each, the GPU figure's count for one head)")
+        return reps * nbytes / dt / 1e9, dt, w.NQ, desc
 
     def pairs(rows):
         if not w.causal:
@@ -204,8 +216,9 @@ def oracle_sample(w, setting: int, target_s: float):
     R = int(min(w.NQ, max(16, probe.size * target_s / max(dt, 1e-6))))
     rows = np.arange(w.NQ - R, w.NQ)
     dt = run(rows)
-    flops = 12 * w.D * pairs(rows)
-    desc = (f"fp64 oracle forward + setting-{setting} backward on the last {R} query rows of head (0,0) "
+    flops = (4 + 8 * len(settings)) * w.D * pairs(rows)
+    which = " + ".join(f"setting-{s}" for s in settings)
+    desc = (f"fp64 oracle forward + {which} backward on the last {R} query rows of head (0,0) "
             f"({pairs(rows)} unmasked pairs, {flops:.3e} counted FLOP)")
     return flops / dt / 1e12, dt, R, desc
 
@@ -234,10 +247,12 @@ def run_reference(args):
     rows = np.arange(w.NQ - R, w.NQ)
     pairs = int(np.minimum(w.NK, rows + (w.NK - w.NQ) + 1).sum()) if w.causal else rows.size * w.NK
 
+    settings = () if decode else ((1, 2) if args.mutual else (args.setting,))
+
     def step():
         O.rows_forward(q1, k1, q2, k2, w.softmax_scale, w.causal, rows)
-        if not decode:
-            O.head_backward_rows(args.setting, q1, k1, q2, k2, w.softmax_scale, w.causal, g, rows)
+        for setting in settings:
+            O.head_backward_rows(setting, q1, k1, q2, k2, w.softmax_scale, w.causal, g, rows)
 
     for _ in range(args.warmup):
         step()
@@ -247,12 +262,14 @@ def run_reference(args):
     dt = time.perf_counter() - t0
     sample = f"fp64 oracle on the last {R} query rows of head (0,0) of {w.name} per step ({pairs} pairs)"
     if decode:
-        nbytes = 2 * w.NK * w.D * 2
+        nbytes = 2 * w.NK * w.D * 2 + 2 * w.NQ * w.D * 2  # the GPU figure's byte count for one head
         value = args.steps * nbytes / dt / 1e9
         metric, unit = "attn-KL split-K decode fwd GB/s (B8 H32 N_K=131072 D128)", "GB/s"
     else:
-        value = args.steps * 12 * w.D * pairs / dt / 1e12
+        value = args.steps * (4 + 8 * len(settings)) * w.D * pairs / dt / 1e12
         metric, unit = "attn-KL fwd+bwd TFLOP/s & ms (H32 D128 N64K causal), % bf16 TC peak", "TFLOP/s"
+        if args.mutual:
+            metric = "attn-KL fwd + both settings' bwd TFLOP/s (mutual case; 20D FLOP per unmasked pair)"
     line = {"impl": "reference", "metric": metric, "value": value, "unit": unit, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
@@ -589,13 +606,10 @@ def run_ours(args):
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu and not args.mutual:
-        if decode:
-            cpu = None
-        else:
-            v, dt, R, desc = oracle_sample(w, args.setting, args.cpu_seconds)
-            cpu = {"value": v, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle", "sample": desc,
-                   "seconds": dt}
+    if rank == 0 and world == 1 and not args.no_cpu:
+        settings = () if decode else ((1, 2) if args.mutual else (args.setting,))
+        v, dt, R, desc = oracle_sample(w, settings, args.cpu_seconds)
+        cpu = {"value": v, "unit": unit, "cores": cpu_cores(), "kind": "oracle", "sample": desc, "seconds": dt}
 
     decode_section = None
     if not decode and not args.no_decode and not args.mutual and args.workload == "kl_b1h32_n65536_d128_causal" and not (
