@@ -65,6 +65,9 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--full", action="store_true",
+                    help="with --impl reference: each step runs the oracle over the whole workload (every head and "
+                         "row), not a sample; minutes at B2 H32 N4096, seconds for decode")
     ap.add_argument("--heads", type=int, default=0, help="override H (smaller cases for profiling)")
     ap.add_argument("--batch", type=int, default=0, help="override B (smaller cases for profiling)")
     ap.add_argument("--nq", type=int, default=0, help="override N_Q")
@@ -230,6 +233,28 @@ def cpu_cores() -> int:
         return os.cpu_count() or 1
 
 
+def blas_threads():
+    """Threads of the BLAS behind numpy (None if it cannot be read)."""
+    try:
+        import threadpoolctl
+        info = [x for x in threadpoolctl.threadpool_info() if x.get("user_api") == "blas"]
+        if info:
+            return int(info[0]["num_threads"])
+    except Exception:
+        pass
+    import ctypes
+    import glob
+    libdir = os.path.join(os.path.dirname(os.path.dirname(np.__file__)), "numpy.libs")
+    for path in sorted(glob.glob(os.path.join(libdir, "*openblas*.so*"))):
+        for name in ("scipy_openblas_get_num_threads64_", "openblas_get_num_threads64_", "openblas_get_num_threads"):
+            try:
+                return int(getattr(ctypes.CDLL(path), name)())
+            except (OSError, AttributeError):
+                continue
+    env = os.environ.get("OPENBLAS_NUM_THREADS") or os.environ.get("OMP_NUM_THREADS")
+    return int(env) if env and env.isdigit() else None
+
+
 # ----------------------------------------------------------------------------- reference arm
 
 def run_reference(args):
@@ -240,29 +265,50 @@ def run_reference(args):
     from oracle import oracle as O
     w = pick_workload(synth, args)
     decode = w.name.startswith("decode")
-    q1, k1, q2, k2 = (synth.bf16_bits_to_f64(synth.head_slice(w, k, 0, 0)) for k in ("q1", "k1", "q2", "k2"))
-    g = synth.upstream_grad(w)[0, 0].astype(np.float64)
-    # rows per step: sized so that one step is ~ a couple of seconds of CPU work
-    R = 64 if not decode else w.NQ
-    rows = np.arange(w.NQ - R, w.NQ)
-    pairs = int(np.minimum(w.NK, rows + (w.NK - w.NQ) + 1).sum()) if w.causal else rows.size * w.NK
-
     settings = () if decode else ((1, 2) if args.mutual else (args.setting,))
+    G = synth.upstream_grad(w).astype(np.float64)
 
-    def step():
-        O.rows_forward(q1, k1, q2, k2, w.softmax_scale, w.causal, rows)
+    def head(b, h):
+        return tuple(synth.bf16_bits_to_f64(synth.head_slice(w, k, b, h)) for k in ("q1", "k1", "q2", "k2"))
+
+    def run_head(ins, g, rows):
+        """The oracle on `rows` of one head; returns its seconds (input generation not timed)."""
+        t = time.perf_counter()
+        O.rows_forward(*ins, w.softmax_scale, w.causal, rows)
         for setting in settings:
-            O.head_backward_rows(setting, q1, k1, q2, k2, w.softmax_scale, w.causal, g, rows)
+            O.head_backward_rows(setting, *ins, w.softmax_scale, w.causal, g, rows)
+        return time.perf_counter() - t
+
+    if args.full:
+        # every head and every query row; one head's inputs are generated at a time
+        rows = np.arange(w.NQ)
+        heads, pairs = w.B * w.H, w.unmasked_pairs()
+
+        def step():
+            return sum(run_head(head(b, h), G[b, h], rows) for b in range(w.B) for h in range(w.H))
+        sample = f"fp64 oracle on the whole of {w.name} per step: all {heads} heads, all {w.NQ} query rows"
+    else:
+        ins, g = head(0, 0), G[0, 0]
+        # rows per step: sized so that one step is ~ a couple of seconds of CPU work
+        R = 64 if not decode else w.NQ
+        rows = np.arange(w.NQ - R, w.NQ)
+        heads = 1
+        pairs = int(np.minimum(w.NK, rows + (w.NK - w.NQ) + 1).sum()) if w.causal else rows.size * w.NK
+
+        def step():
+            return run_head(ins, g, rows)
+        sample = f"fp64 oracle on the last {R} query rows of head (0,0) of {w.name} per step ({pairs} pairs)"
 
     for _ in range(args.warmup):
         step()
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        step()
-    dt = time.perf_counter() - t0
-    sample = f"fp64 oracle on the last {R} query rows of head (0,0) of {w.name} per step ({pairs} pairs)"
+    dt = sum(step() for _ in range(args.steps))
+    # the whole workload's oracle time at this step's rate (an extrapolation unless --full)
     if decode:
-        nbytes = 2 * w.NK * w.D * 2 + 2 * w.NQ * w.D * 2  # the GPU figure's byte count for one head
+        full_s = dt / args.steps * (w.B * w.H) / heads
+    else:
+        full_s = dt / args.steps * w.unmasked_pairs() / pairs
+    if decode:
+        nbytes = heads * (2 * w.NK * w.D * 2 + 2 * w.NQ * w.D * 2)  # the GPU figure's byte count per head
         value = args.steps * nbytes / dt / 1e9
         metric, unit = "attn-KL split-K decode fwd GB/s (B8 H32 N_K=131072 D128)", "GB/s"
     else:
@@ -280,7 +326,10 @@ def run_reference(args):
                        "path": ("oracle rows_forward" if decode else "oracle rows_forward + head_backward_rows"),
                        "per_gpu_units": "a bounded sample of the workload per step (see cpu_baseline.sample)",
                        "parallelism": "replicas1"},
-            "cpu_baseline": {"value": value, "unit": unit, "cores": cpu_cores(), "kind": "oracle", "sample": sample},
+            "cpu_baseline": {"value": value, "unit": unit, "cores": cpu_cores(), "blas_threads": blas_threads(),
+                             "kind": "oracle", "sample": sample,
+                             "full_workload_s": full_s,
+                             "full_workload_s_is": "measured" if args.full else "extrapolated from the sample's rate"},
             "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
     return 0
@@ -609,7 +658,8 @@ def run_ours(args):
     if rank == 0 and world == 1 and not args.no_cpu:
         settings = () if decode else ((1, 2) if args.mutual else (args.setting,))
         v, dt, R, desc = oracle_sample(w, settings, args.cpu_seconds)
-        cpu = {"value": v, "unit": unit, "cores": cpu_cores(), "kind": "oracle", "sample": desc, "seconds": dt}
+        cpu = {"value": v, "unit": unit, "cores": cpu_cores(), "blas_threads": blas_threads(), "kind": "oracle",
+               "sample": desc, "seconds": dt}
 
     decode_section = None
     if not decode and not args.no_decode and not args.mutual and args.workload == "kl_b1h32_n65536_d128_causal" and not (
