@@ -67,7 +67,8 @@ def parse():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--full", action="store_true",
                     help="with --impl reference: each step runs the oracle over the whole workload (every head and "
-                         "row), not a sample; minutes at B2 H32 N4096, seconds for decode")
+                         "row), not a sample; about a minute at B2 H32 N4096, several for decode, where drawing "
+                         "the 256 heads' inputs dominates")
     ap.add_argument("--heads", type=int, default=0, help="override H (smaller cases for profiling)")
     ap.add_argument("--batch", type=int, default=0, help="override B (smaller cases for profiling)")
     ap.add_argument("--nq", type=int, default=0, help="override N_Q")
