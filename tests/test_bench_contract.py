@@ -60,3 +60,24 @@ def test_reference_arm_sample_extrapolates():
     sample_pairs = sum(min(4096, i + 1) for i in range(4096 - 64, 4096))
     ratio = 64 * 4096 * 4097 // 2 / sample_pairs
     assert cb["full_workload_s"] == pytest.approx(d["ms_per_step"] / 1e3 * ratio, rel=1e-9)
+
+
+def test_cpu_baseline_sampler_covers_every_kind_of_workload():
+    """The GPU arm's cpu_baseline helper: forward + one backward, forward + both backwards, and decode (bytes)."""
+    sys.path.insert(0, ROOT)
+    import bench
+    from attention_kl_divergence_streamkl_gb300 import synth
+
+    w = synth.WORKLOADS["kl_b1h1_n128_d64"]
+    v1, dt1, r1, d1 = bench.oracle_sample(w, (1,), 0.05)
+    v12, dt12, r12, d12 = bench.oracle_sample(w, (1, 2), 0.05)
+    assert v1 > 0 and v12 > 0 and 16 <= r1 <= 128 and 16 <= r12 <= 128
+    assert "setting-1 backward" in d1 and "setting-1 + setting-2 backward" in d12
+    # counted FLOP per unmasked pair: 12D for one backward, 20D for both (rows r of 128 keys each, non-causal)
+    assert v1 * 1e12 * dt1 == pytest.approx(12 * 64 * r1 * 128, rel=1e-9)
+    assert v12 * 1e12 * dt12 == pytest.approx(20 * 64 * r12 * 128, rel=1e-9)
+    wd = synth.WORKLOADS["decode_b8h32_nq1_nk131072_d128"]
+    vd, dtd, rd, dd = bench.oracle_sample(wd, (), 0.05)
+    assert vd > 0 and rd == 1 and "K1, K2, Q1 and Q2" in dd
+    b = bench.blas_threads()
+    assert b is None or b >= 1
