@@ -81,3 +81,33 @@ def test_cpu_baseline_sampler_covers_every_kind_of_workload():
     assert vd > 0 and rd == 1 and "K1, K2, Q1 and Q2" in dd
     b = bench.blas_threads()
     assert b is None or b >= 1
+
+
+GPU_KEYS = KEYS - {"impl"} | {"roofline", "clocks", "gpu_launches", "per_kernel_ms", "extra_hbm"}
+
+
+def _run_ours(*args):
+    r = subprocess.run([sys.executable, "bench.py", *args], cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    return json.loads(lines[0])
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("extra,unit", [(("--workload", "kl_b2h32_n4096_d128_causal"), "TFLOP/s"),
+                                        (("--workload", "kl_b2h32_n4096_d128_causal", "--mutual"), "TFLOP/s"),
+                                        (("--workload", "decode_b8h32_nq4_nk131072_d128"), "GB/s")])
+def test_gpu_arm_line(extra, unit):
+    """The GPU arm's JSON line on small workloads: every contract key, a roofline for the dominant kernel, a
+    positive end-to-end figure with its copies counted, and a launch count."""
+    d = _run_ours(*extra, "--steps", "3", "--warmup", "3", "--cpu-seconds", "0.5")
+    assert GPU_KEYS <= set(d), GPU_KEYS - set(d)
+    assert d["unit"] == unit and d["value"] > 0 and d["n_gpus"] == 1 and d["steps"] == 3 and d["warmup"] == 3
+    roof = d["roofline"]
+    assert roof["bound"] in ("tensor", "hbm") and roof["achieved"] > 0 and roof["peak"] > 0
+    assert roof["frac"] == pytest.approx(roof["achieved"] / roof["peak"], rel=1e-6)
+    e2e = d["e2e"]
+    assert e2e["value"] > 0 and e2e["unit"] == unit and e2e["h2d_bytes_per_step"] > 0 and e2e["d2h_bytes_per_step"] > 0
+    assert d["gpu_launches"] >= 3 * 1 and d["cpu_baseline"]["value"] > 0 and d["cpu_baseline"]["cores"] >= 1
+    assert {"sm_mhz", "sm_max_mhz", "reasons"} <= set(d["clocks"])
